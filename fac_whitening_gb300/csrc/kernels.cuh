@@ -1,0 +1,115 @@
+// Internal launcher declarations of libgift (host side of each kernel file).
+#pragma once
+
+#include "common.cuh"
+
+namespace gift {
+
+struct Launch {
+  cudaStream_t stream;
+  int sms;       // streaming multiprocessors of the device
+  int *status;   // caller's device status word (nullable)
+};
+
+struct ReduceArgs {
+  const void *codes[kMaxReplicas];
+  const void *scales[kMaxReplicas];
+  const float *tscales[kMaxReplicas];
+};
+
+// ---- quant.cu ---------------------------------------------------------------------------
+cudaError_t launch_amax(const Launch &L, const float *x, const float *r, size_t n, float *amax_accum);
+cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *r, size_t n, const float *amax,
+                               uint8_t *codes, float *scale, float *amax_out, float *tout);
+cudaError_t launch_pack_f32(const Launch &L, const float *x, float *r, size_t n, float *out, float *tout);
+// mode 0: pack, 1: amax only (max-accumulated into amax_out), 2: count boundary hits
+cudaError_t launch_block128(const Launch &L, int fmt, int mode, const float *x, float *r, int d_out, int d_in,
+                            const float *amax_in, uint8_t *codes, float *scales, float *amax_out, float *tout,
+                            unsigned long long *counts);
+cudaError_t launch_pack_nvfp4(const Launch &L, const float *x, float *r, size_t n, const float *amax,
+                              uint8_t *codes, uint8_t *bscale, float *tscale, float *amax_out, float *tout);
+cudaError_t launch_hits_tensor(const Launch &L, int fmt, const float *x, size_t n, const float *amax,
+                               unsigned long long *counts);
+cudaError_t launch_reduce(const Launch &L, const ReduceArgs &a, int R, int fmt, int scaling, int d_out, int d_in,
+                          float *out);
+
+// ---- lowrank.cu -------------------------------------------------------------------------
+// Split-K projection P = X U (d_out x 32, zero-padded beyond rank); partials to `part`.
+int lr_proj_splits(int sms, int d_out, int d_in);
+cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in, const float *U, int rank,
+                           float *part, int nsplit);
+// Pc[row][k] = c_k * sum_s part[s][row][k]; c from (mu, sigma), inverse = map-back coefficients.
+cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
+                               const float *sigma, int rank, bool inverse, float *Pc);
+// Fused apply V = alpha X + Pc U^T (+ R), alpha = sigma^-1/2 (or sigma^1/2 for the map back).
+enum LrEpi { LR_AMAX = 0, LR_PACK_TENSOR = 1, LR_BLOCK = 2, LR_NVFP4 = 3, LR_STORE = 4, LR_BLOCK_AMAX = 5 };
+struct LrApply {
+  const float *X;
+  const float *U;
+  const float *Pc;
+  const float *sigma;
+  int rank, d_out, d_in;
+  bool inverse;
+  float *R;                 // residual (nullable)
+  float *tout;              // transformed copy (nullable)
+  const float *amax_in;     // shared amax (nullable)
+  float *amax_ws;           // LR_AMAX / LR_BLOCK_AMAX: max-accumulated; LR_PACK_TENSOR / NVFP4: read
+  uint8_t *codes;
+  void *scales;
+  float *tscale;
+  float *amax_out;
+  float *out;               // LR_STORE
+};
+cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
+
+// ---- linalg.cu --------------------------------------------------------------------------
+// C[M x N] = alpha * op(A) op(B), FP32 accumulate.  op(A) = A (M x K, lda) or A^T (A is K x M).
+// op(B) = B (K x N, ldb) or B^T (B is N x K).  a_lower: op(A)[m][k] = 0 for k > m;
+// b_lower_t: op(B)[k][n] = 0 for k > n.  lower_tiles: only tiles with n0 <= m0 (square tiles).
+struct GemmArgs {
+  const void *A;
+  const void *B;
+  float *C;
+  int M, N, K, lda, ldb, ldc;
+  bool transA, transB;
+  bool a_bf16, b_bf16;
+  bool a_lower, b_lower_t, lower_tiles;
+  float alpha;
+};
+cudaError_t launch_sgemm(const Launch &L, const GemmArgs &g);
+cudaError_t launch_sgemm_splitk(const Launch &L, const GemmArgs &g, float *parts, int splits);
+size_t sgemm_splitk_parts(int M, int ldc, int splits);
+// C = alpha * op(A) op(B) + beta * C in FP64 with float or double operands, split-K slices
+// written to C + z * slice_stride (summed by launch_sum_slices).
+struct DgemmArgs {
+  const void *A;
+  const void *B;
+  double *C;
+  int M, N, K, lda, ldb, ldc;
+  bool transA, transB;
+  bool a_f32, b_f32;
+  double alpha, beta;
+  int splits;
+  size_t slice_stride;
+};
+cudaError_t launch_dgemm(const Launch &L, const DgemmArgs &g);
+cudaError_t launch_sum_slices(const Launch &L, const double *parts, int splits, size_t slice_stride, size_t n,
+                              double *out, double scale);
+cudaError_t launch_mirror_lower(const Launch &L, float *A, int n);
+cudaError_t launch_f32_to_f64(const Launch &L, const float *x, double *y, size_t n);
+cudaError_t launch_f64_to_f32(const Launch &L, const double *x, float *y, size_t n, bool zero_upper, int n_cols);
+// Cholesky A = L L^T and L^-1 in FP64 (A is overwritten by L, Linv receives L^-1), n x n.
+cudaError_t launch_chol_inv(const Launch &L, double *A, double *Linv, int n, double *work);
+size_t chol_inv_work_doubles(int n);
+
+// ---- factor.cu --------------------------------------------------------------------------
+cudaError_t launch_philox_gaussian(const Launch &L, float *out, size_t n, uint64_t seed);
+cudaError_t launch_trace(const Launch &L, const float *A, int n, double *tr);
+cudaError_t launch_small_chol_rinv(const Launch &L, const double *G, int k, double *Rinv);
+cudaError_t launch_jacobi(const Launch &L, const double *B, int k, double *evals, double *V);
+cudaError_t launch_lowrank_outputs(const Launch &L, const float *Q, int d_in, int k, const double *V,
+                                   const double *evals, const double *trace, int rank, float *U, float *mu,
+                                   float *sigma);
+cudaError_t launch_eye(const Launch &L, float *Q, int n);
+
+}  // namespace gift

@@ -1,0 +1,256 @@
+/*
+ * gift.h — C ABI of libgift, a GB300 (sm_103a) implementation of GIFT's
+ * per-layer gradient codec.
+ *
+ * GIFT (Geometry-Informed low-precision gradient communication) whitens a weight
+ * gradient with the layer's K-FAC input factor before it is quantised to FP8 or
+ * NVFP4 for the data-parallel all-reduce, and maps the averaged result back
+ * afterwards.  Sources (cited by page title and section):
+ *   [notes]    "GIFT 阅读笔记:量化用的坐标系,比量化器本身更重要" (GIFT reading notes,
+ *              zhongzhuzhou.org): prerequisites ("What FP8 is", "K-FAC"), core idea
+ *              steps 1-3 with eqs. (4)-(14), the three simplifications with eqs.
+ *              (15)-(17) and the profiling procedure, Algorithm 1.
+ *   [abstract] "GIFT: Geometry-Informed Low-precision Gradient Communication for
+ *              LLM Pretraining" (shd-paper.top), abstract: FP8 and NVFP4 formats.
+ *
+ * Conventions for every entry point
+ *   Layout     Matrices are row-major and contiguous.  A gradient W is d_out x d_in
+ *              (leading dimension d_in); activations a are T x d_in; delta is T x d_out.
+ *   Ownership  The caller owns every buffer: inputs, outputs, factor storage,
+ *              workspace (size from gift_workspace_bytes) and the status word.  The
+ *              library never allocates device memory and never frees caller memory.
+ *              Pointers documented as "device" must point to memory of the device the
+ *              context was created for, and that device must be current; pointer
+ *              arrays ("host array of device pointers") live in host memory.
+ *   Streams    Every call only enqueues work on the caller's stream and returns; no
+ *              call synchronises the device.  Results are valid once the stream has
+ *              reached the call.
+ *   Errors     Two channels.  (1) The return value reports argument validation and
+ *              launch failures synchronously (nothing is enqueued on an error other
+ *              than GIFT_ERR_CUDA, whose partial work is undefined).  (2) Conditions
+ *              only the device can see (a non-finite input, a factor that is not
+ *              positive definite, an eigensolver that did not converge) are written
+ *              into the caller's device word `d_status` with compare-and-swap from 0:
+ *              the first error wins, the library never clears the word.  Pass
+ *              d_status = NULL to ignore them.  Outputs are undefined when the word
+ *              is non-zero.
+ *   Alignment  Any alignment works; 16-byte aligned buffers with d_in a multiple of
+ *              4 (FP32) or 16 (codes) take the vectorised paths.
+ *   Aliasing   Outputs must not alias inputs unless a parameter says otherwise.
+ */
+#ifndef GIFT_H_
+#define GIFT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GIFT_VERSION_MAJOR 0
+#define GIFT_VERSION_MINOR 1
+
+typedef enum {
+  GIFT_OK = 0,
+  GIFT_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum, workspace too small */
+  GIFT_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination                 */
+  GIFT_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed                  */
+  GIFT_ERR_NONFINITE = 4,     /* device: NaN or Inf in the tensor being scaled         */
+  GIFT_ERR_NOT_PD = 5,        /* device: Cholesky pivot <= 0, or sigma/mu <= 0         */
+  GIFT_ERR_TIMEOUT = 6,       /* device: a bounded wait gave up                        */
+  GIFT_ERR_NOT_CONVERGED = 7  /* device: the eigensolver did not converge              */
+} gift_status;
+
+/* Element formats ([notes] prerequisites "What FP8 is"; [abstract] NVFP4).
+ *  F32   : no quantisation, codes are the FP32 values (lossless round-trip tests).
+ *  E4M3  : 1 sign, 4 exponent (bias 7), 3 mantissa bits; largest finite 448, no Inf.
+ *  E5M2  : 1 sign, 5 exponent (bias 15), 2 mantissa bits; largest finite 57344.
+ *  NVFP4 : E2M1 codes (largest 6), two per byte with the even column in the low
+ *          nibble; one E4M3 scale byte per 16 consecutive elements of a row
+ *          (scales[d_out][d_in/16]); one FP32 tensor scale.  Needs d_in % 16 == 0.
+ * Rounding is round-to-nearest-even with saturation to the largest finite value;
+ * the sign of zero is kept. */
+typedef enum { GIFT_FMT_F32 = 0, GIFT_FMT_E4M3 = 1, GIFT_FMT_E5M2 = 2, GIFT_FMT_NVFP4 = 3 } gift_format;
+
+/* Scale groups for FP8 ([notes] "What FP8 is": per tensor or per block).
+ *  TENSOR   : one FP32 scale, scales[1].
+ *  BLOCK128 : one FP32 scale per 128 x 128 tile, scales[ceil(d_out/128)][ceil(d_in/128)],
+ *             edge tiles clipped.
+ * NVFP4 ignores this (its groups are fixed); F32 has no scales. */
+typedef enum { GIFT_SCALE_TENSOR = 0, GIFT_SCALE_BLOCK128 = 1 } gift_scaling;
+
+/* Coordinate transforms ([notes] core idea eqs. (11), (14); simplification 1 eq. (16);
+ * simplification 2 eq. (17)).
+ *  IDENTITY        : the Euclidean path, W~ = W.
+ *  LOWRANK         : W~ = W T_A, T_A = sigma^-1/2 I + U (diag(mu^-1/2) - sigma^-1/2) U^T,
+ *                    A ~ U diag(mu - sigma) U^T + sigma I with mu the top `rank`
+ *                    eigenvalues of A; decode applies T_A^-1.
+ *  CHOL_INPUT      : W~ = W L_A^-T, decode W^ = X L_A^T.
+ *  CHOL_TWO_SIDED  : W~ = L_G^-1 W L_A^-T, decode W^ = L_G X L_A^T. */
+typedef enum {
+  GIFT_XF_IDENTITY = 0,
+  GIFT_XF_LOWRANK = 1,
+  GIFT_XF_CHOL_INPUT = 2,
+  GIFT_XF_CHOL_TWO_SIDED = 3
+} gift_xform;
+
+/* Arithmetic of the transforms.  FP32: FP32 arithmetic, relative Frobenius error of
+ * the transformed and decoded tensors within 1e-5 of exact.  TC: reduced-precision
+ * tensor-core arithmetic, within 2e-2 (accepted; currently runs the FP32 path). */
+typedef enum { GIFT_PREC_FP32 = 0, GIFT_PREC_TC = 1 } gift_precision;
+
+/* Element type of activation inputs. */
+typedef enum { GIFT_DT_F32 = 0, GIFT_DT_BF16 = 1 } gift_dtype;
+
+/* One layer's factor: every pointer is device memory owned by the caller.
+ *  LOWRANK        : U (d_in x rank, row-major, orthonormal columns), mu (rank values,
+ *                   descending, the top eigenvalues of A), sigma (1 value).
+ *  CHOL_INPUT     : LA and LAinv (d_in x d_in, lower triangular, upper part zero).
+ *  CHOL_TWO_SIDED : as CHOL_INPUT plus LG and LGinv (d_out x d_out).
+ * Unused pointers may be NULL.  1 <= rank <= 32 and rank <= d_in. */
+typedef struct {
+  gift_xform kind;
+  int d_in, d_out, rank;
+  float *U;
+  float *mu;
+  float *sigma;
+  float *LA, *LAinv;
+  float *LG, *LGinv;
+} gift_factor;
+
+/* Opaque host context: device properties and tuning; holds no device memory and no
+ * per-call state, so calls on different streams may run concurrently. */
+typedef struct gift_ctx gift_ctx;
+
+/* Operations for gift_workspace_bytes. */
+typedef enum {
+  GIFT_OP_FACTOR_UPDATE = 0,
+  GIFT_OP_ENCODE = 1,
+  GIFT_OP_DECODE = 2,
+  GIFT_OP_AMAX = 3
+} gift_op;
+
+/* Tunables for gift_set_option. */
+typedef enum {
+  GIFT_OPT_SUBSPACE_ITERS = 0  /* power iterations of the rank-r sketch (default 10, 1..64) */
+} gift_option;
+
+/* Create a context for CUDA device `device` (queries its SM count).  Returns
+ * GIFT_ERR_INVALID_ARG for a NULL ctx, GIFT_ERR_CUDA when the device cannot be queried. */
+gift_status gift_create(gift_ctx **ctx, int device);
+void gift_destroy(gift_ctx *ctx);
+gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value);
+const char *gift_status_string(gift_status s);
+int gift_version(void); /* major * 1000 + minor */
+
+/* Bytes of caller-provided device workspace an operation needs (0 if none).
+ * Host-only; returns (size_t)-1 for invalid arguments.  T is used by
+ * GIFT_OP_FACTOR_UPDATE only, rank by the LOWRANK kind only. */
+size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gift_format fmt,
+                            gift_scaling scaling, int d_out, int d_in, int T, int rank);
+
+/* Sizes of one encoded tensor: code bytes, and the number of scale entries (FP32 entries
+ * for E4M3/E5M2, E4M3 bytes for NVFP4, 0 for F32).  Host-only. */
+gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, int d_in,
+                            size_t *code_bytes, size_t *scale_count);
+
+/* Factor refresh ([notes] eq. (4): A = E[a a^T] ~ a^T a / T; core idea step 2 eq. (7):
+ * Cholesky; simplification 2 eq. (17): rank-r eigen approximation; Algorithm 1 refreshes
+ * it every K steps).
+ *  a      : device, T x d_in activations of type a_dt.
+ *  delta  : device, T x d_out output gradients of type d_dt (CHOL_TWO_SIDED only, else NULL).
+ *  f      : f->kind selects the factor; its buffers receive the result.
+ *  LOWRANK: randomised block subspace iteration on A with a seeded Gaussian start of
+ *           k = min(64, d_in) columns (Philox4x32-10 from `seed`), GIFT_OPT_SUBSPACE_ITERS
+ *           power steps with CholQR2 re-orthonormalisation, Rayleigh-Ritz and a one-CTA
+ *           Jacobi eigensolve; U = Q V[:, :rank]; sigma = (tr A - sum mu) / (d_in - rank)
+ *           (sigma = 1 when rank == d_in).  d_status: NOT_PD when sigma or a mu is <= 0,
+ *           NOT_CONVERGED when the Jacobi sweeps do not converge.
+ *  CHOL_* : A (and G) are formed in FP32 and factored in FP64; L and L^-1 are stored in
+ *           FP32.  d_status: NOT_PD on a non-positive pivot.
+ *  ws     : device workspace of gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ...) bytes.
+ * Returns INVALID_ARG on null pointers, T < 1, rank outside [1, min(32, d_in)]. */
+gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
+                               const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
+                               void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* Amax of the tensor that gift_encode would quantise (the transformed gradient, plus the
+ * residual when one is given), max-accumulated into amax_accum: the AllReduceMax of the
+ * scale in Algorithm 1, modelled on one GPU by calling this once per replica on one
+ * accumulator the caller set to 0 beforehand.  amax_accum holds 1 float (TENSOR, NVFP4)
+ * or ceil(d_out/128) x ceil(d_in/128) floats (BLOCK128).  d_status: NONFINITE. */
+gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
+                      gift_format fmt, gift_scaling scaling, gift_precision prec,
+                      const float *residual, float *amax_accum, void *ws, size_t ws_bytes,
+                      int *d_status, cudaStream_t stream);
+
+/* Encode one gradient ([notes] Algorithm 1: whiten, add the error-feedback residual,
+ * Scale, Q; eq. (13) CommFP8 input side).
+ *  f         : NULL or kind IDENTITY for the Euclidean path.
+ *  W         : device, d_out x d_in FP32 gradient.
+ *  amax_in   : device, nullable.  When given, the scale uses this amax (shared scale of the
+ *              Euclidean path) instead of the tensor's own: 1 float (TENSOR, NVFP4) or one
+ *              per 128 x 128 block.
+ *  residual  : device, nullable, d_out x d_in FP32 error-feedback buffer R in whitened
+ *              coordinates: U~ = W~ + R is quantised, then R <- U~ - Dequantize(Q(U~)).
+ *  codes     : device, gift_code_sizes bytes (F32: d_out*d_in floats).
+ *  scales    : device, gift_code_sizes entries (FP32, or E4M3 bytes for NVFP4).
+ *  tensor_scale : device, 1 float, NVFP4 only (else NULL).
+ *  transformed_out : device, nullable, receives U~ in FP32 (parity and fidelity checks).
+ *  amax_out  : device, nullable, receives the amax used (same shape as amax_in).
+ *  Scale rule: s = amax / FMAX stored, elements scaled by m = FMAX / amax (two FP32
+ *  divisions, FMAX = 448 or 57344); amax = 0 gives s = m = 0; m beyond FP32 is clamped.
+ *  NVFP4: s_t = amax / 2688; per group of 16, e = E4M3(group_amax / (6 s_t)),
+ *  r = 1 / (e s_t), code = E2M1(x r).
+ *  d_status: NONFINITE when the tensor holds NaN/Inf.  W must not alias codes or
+ *  residual. */
+gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
+                        gift_format fmt, gift_scaling scaling, gift_precision prec,
+                        const float *amax_in, float *residual, void *codes, void *scales,
+                        float *tensor_scale, float *transformed_out, float *amax_out,
+                        void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* Replica reduce: out = (sum_r deq_r) / R in FP32, adding replicas in order r = 0..R-1
+ * with each replica dequantised with its own scale ([notes] eq. (1) data-parallel average;
+ * Algorithm 1 AllReduceSum, Dequantize, divide by N — modelled on one GPU over R code
+ * buffers held in this GPU's memory).
+ *  codes, scales, tensor_scales : host arrays of R device pointers (tensor_scales only for
+ *                                 NVFP4, may be NULL otherwise; scales NULL for F32).
+ *  avg_out : device, d_out x d_in FP32.  1 <= R <= 64. */
+gift_status gift_replica_reduce(gift_ctx *ctx, int R, const void *const *codes,
+                                const void *const *scales, const float *const *tensor_scales,
+                                gift_format fmt, gift_scaling scaling, int d_out, int d_in,
+                                float *avg_out, int *d_status, cudaStream_t stream);
+
+/* Decode: dequantise (when `in` holds codes) and map back to the gradient's coordinates
+ * ([notes] eq. (14); Algorithm 1 multiplies by L_A^T).
+ *  in         : device; codes of `fmt` when in_is_codes != 0 (with scales / tensor_scale as
+ *               written by gift_encode), else a d_out x d_in FP32 tensor in whitened
+ *               coordinates (for example gift_replica_reduce's output).
+ *  W_out      : device, d_out x d_in FP32.  Must not alias `in`.
+ *  ws         : gift_workspace_bytes(GIFT_OP_DECODE, ...) bytes. */
+gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int in_is_codes,
+                        const void *scales, const float *tensor_scale, gift_format fmt,
+                        gift_scaling scaling, gift_precision prec, int d_out, int d_in, float *W_out,
+                        void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* Boundary-hit profiler ([notes] simplification 3: encode the flattened gradient with the
+ * scale that would be used and count codes on the upper or lower boundary of the FP8
+ * format).  Euclidean encode with the tensor's own scale (per tensor or per block);
+ * adds into d_counts[0] the number of codes whose magnitude is the largest finite code,
+ * into d_counts[1] the number of non-zero elements whose code is zero, and into
+ * d_counts[2] the number of elements.  Counts accumulate across calls (a profiling
+ * window); the caller zeroes them.  fmt: E4M3 or E5M2.
+ *  ws : gift_workspace_bytes(GIFT_OP_AMAX, IDENTITY, ...) bytes (one amax word).
+ *  d_status: NONFINITE. */
+gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int d_in,
+                                   gift_format fmt, gift_scaling scaling,
+                                   unsigned long long *d_counts, void *ws, size_t ws_bytes,
+                                   int *d_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GIFT_H_ */
