@@ -361,13 +361,13 @@ def dequantize_any(q, fmt: str, scaling: str = "tensor") -> np.ndarray:
 # ======================================================================================
 
 def replica_reduce(qs, fmt: str, scaling: str = "tensor") -> np.ndarray:
-    """out = (sum_r deq_r) / R with FP32 accumulation in replica order r = 0..R-1."""
+    """out = (deq_0 + deq_1 + ... + deq_{R-1}) / R, FP32 additions left to right."""
     R = len(qs)
     acc = None
     for q in qs:
         d = dequantize_any(q, fmt, scaling)
+        # acc starts at replica 0's values (not at 0 + deq_0, which would turn -0 into +0)
         acc = d.copy() if acc is None else (acc + d).astype(np.float32)
-        # the first add is 0 + d = d exactly, so starting from d is the same as from 0
     return (acc / F32(R)).astype(np.float32)
 
 
@@ -636,11 +636,26 @@ def chol_two_sided_unwhiten(X, LG, LA) -> np.ndarray:
     return np.asarray(LG, dtype=np.float64) @ np.asarray(X, dtype=np.float64) @ np.asarray(LA, dtype=np.float64).T
 
 
-class Xform:
-    """A transform: kind in {identity, lowrank, chol_input, chol_two_sided} and its factor."""
+def chol_whiten_with_inverses(W, LAinv, LGinv=None) -> np.ndarray:
+    """W~ = L_G^-1 W L_A^-T written with given inverse factors (eq. (11) as printed, with
+    L^-1; the input-side form of eq. (16) when LGinv is None)."""
+    X = np.asarray(W, dtype=np.float64) @ np.asarray(LAinv, dtype=np.float64).T
+    if LGinv is not None:
+        X = np.asarray(LGinv, dtype=np.float64) @ X
+    return X
 
-    def __init__(self, kind, F=None, LA=None, LG=None):
+
+class Xform:
+    """A transform: kind in {identity, lowrank, chol_input, chol_two_sided} and its factor.
+
+    For the Cholesky kinds the factor may carry the inverse factors L^-1 explicitly
+    (as libgift's factor does); the whitening then multiplies by them, otherwise it
+    solves with L.
+    """
+
+    def __init__(self, kind, F=None, LA=None, LG=None, LAinv=None, LGinv=None):
         self.kind, self.F, self.LA, self.LG = kind, F, LA, LG
+        self.LAinv, self.LGinv = LAinv, LGinv
 
     def whiten(self, W):
         if self.kind == "identity":
@@ -648,7 +663,11 @@ class Xform:
         if self.kind == "lowrank":
             return lowrank_whiten(W, self.F)
         if self.kind == "chol_input":
+            if self.LAinv is not None:
+                return chol_whiten_with_inverses(W, self.LAinv)
             return chol_input_whiten(W, self.LA)
+        if self.LAinv is not None and self.LGinv is not None:
+            return chol_whiten_with_inverses(W, self.LAinv, self.LGinv)
         return chol_two_sided_whiten(W, self.LG, self.LA)
 
     def unwhiten(self, X):

@@ -339,6 +339,17 @@ def test_eq12_two_sided_transform_kronecker_form():
                                rtol=1e-10, atol=1e-12)
 
 
+def test_whitening_with_given_inverses_matches_solves():
+    # eq. (11) written with L^-1 (factor carries the inverses) equals the triangular solves
+    rng = np.random.default_rng(26)
+    LA, LG = O.cholesky(_spd(30, 27, 1e4)), O.cholesky(_spd(7, 28, 1e2))
+    W = rng.standard_normal((7, 30))
+    np.testing.assert_allclose(O.chol_whiten_with_inverses(W, O.lower_inverse(LA)), O.chol_input_whiten(W, LA),
+                               rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(O.chol_whiten_with_inverses(W, O.lower_inverse(LA), O.lower_inverse(LG)),
+                               O.chol_two_sided_whiten(W, LG, LA), rtol=1e-10, atol=1e-10)
+
+
 @pytest.mark.parametrize("kind", ["identity", "lowrank", "chol_input", "chol_two_sided"])
 def test_eq14_map_back_inverts_eq11(kind):
     # with a lossless format the map back is exact (common confusions: lossless GIFT = baseline)
