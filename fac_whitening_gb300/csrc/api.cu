@@ -1,0 +1,618 @@
+// C ABI of libgift: argument validation, workspace layout and kernel sequencing.
+//
+// Each entry point validates its arguments on the host, carves the caller's workspace
+// with the same layout function that gift_workspace_bytes uses, and enqueues kernels on
+// the caller's stream.  No call allocates or frees device memory and no call synchronises.
+#include <cstdlib>
+#include <cstring>
+
+#include "kernels.cuh"
+
+struct gift_ctx {
+  int device;
+  int sms;
+  int subspace_iters;
+};
+
+using namespace gift;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+// Bump allocator over the caller's workspace; with base == nullptr it only measures.
+struct Carve {
+  char *base;
+  size_t off = 0;
+  explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+  template <typename T>
+  T *take(size_t count) {
+    off = (off + kAlign - 1) / kAlign * kAlign;
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+bool valid_fmt(gift_format f) { return f >= GIFT_FMT_F32 && f <= GIFT_FMT_NVFP4; }
+bool valid_scaling(gift_scaling s) { return s == GIFT_SCALE_TENSOR || s == GIFT_SCALE_BLOCK128; }
+bool valid_kind(gift_xform k) { return k >= GIFT_XF_IDENTITY && k <= GIFT_XF_CHOL_TWO_SIDED; }
+
+// ---- codec workspace (encode / amax / decode) -----------------------------------------
+struct CodecWs {
+  float *amax = nullptr;   // one word (64 floats reserved)
+  float *part = nullptr;   // LOWRANK: nsplit x d_out x 32 slice partials of X U
+  float *Pc = nullptr;     // LOWRANK: d_out x 32
+  float *xbuf = nullptr;   // transformed tensor (CHOL encode) or dequantised input (decode)
+  float *tbuf = nullptr;   // CHOL_TWO_SIDED intermediate
+  int nsplit = 0;
+  size_t bytes = 0;
+};
+
+CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out, int d_in) {
+  CodecWs w;
+  Carve c(base);
+  const size_t n = (size_t)d_out * d_in;
+  w.amax = c.take<float>(64);
+  if (kind == GIFT_XF_LOWRANK) {
+    w.nsplit = lr_proj_splits(sms, d_out, d_in);
+    w.part = c.take<float>((size_t)w.nsplit * d_out * 32);
+    w.Pc = c.take<float>((size_t)d_out * 32);
+  }
+  if (kind != GIFT_XF_IDENTITY) {
+    if (op == GIFT_OP_DECODE || kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED)
+      w.xbuf = c.take<float>(n);
+    if (kind == GIFT_XF_CHOL_TWO_SIDED) w.tbuf = c.take<float>(n);
+  }
+  w.bytes = c.off;
+  return w;
+}
+
+// ---- factor-update workspace -------------------------------------------------------------
+struct FactorWs {
+  float *A = nullptr;       // d_in x d_in
+  // LOWRANK
+  int k = 0, gsplits = 1, ysplits = 1;
+  float *Y = nullptr, *Q = nullptr, *yparts = nullptr;
+  double *Q64 = nullptr, *Gp = nullptr, *G = nullptr, *Rinv = nullptr, *V = nullptr, *ev = nullptr, *tr = nullptr;
+  // CHOL
+  double *A64 = nullptr, *Ai64 = nullptr, *work = nullptr;
+  float *Gf = nullptr;
+  double *G64 = nullptr, *Gi64 = nullptr;
+  size_t bytes = 0;
+};
+
+FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in) {
+  FactorWs w;
+  Carve c(base);
+  w.A = c.take<float>((size_t)d_in * d_in);
+  if (kind == GIFT_XF_LOWRANK) {
+    w.k = d_in < 64 ? d_in : 64;
+    w.gsplits = d_in / 256;
+    if (w.gsplits < 1) w.gsplits = 1;
+    if (w.gsplits > 64) w.gsplits = 64;
+    const int rowtiles = (d_in + 127) / 128;
+    w.ysplits = (2 * sms + rowtiles - 1) / rowtiles;
+    const int maxs = (d_in + 255) / 256;
+    if (w.ysplits > maxs) w.ysplits = maxs;
+    if (w.ysplits < 1) w.ysplits = 1;
+    const size_t dk = (size_t)d_in * w.k;
+    w.Y = c.take<float>(dk);
+    w.Q = c.take<float>(dk);
+    w.yparts = c.take<float>(sgemm_splitk_parts(d_in, w.k, w.ysplits));
+    w.Q64 = c.take<double>(dk);
+    w.Gp = c.take<double>((size_t)w.gsplits * w.k * w.k);
+    w.G = c.take<double>(64 * 64);
+    w.Rinv = c.take<double>(64 * 64);
+    w.V = c.take<double>(64 * 64);
+    w.ev = c.take<double>(64);
+    w.tr = c.take<double>(1);
+  } else if (kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED) {
+    const int nmax = d_in > d_out ? d_in : d_out;
+    w.A64 = c.take<double>((size_t)d_in * d_in);
+    w.Ai64 = c.take<double>((size_t)d_in * d_in);
+    w.work = c.take<double>(chol_inv_work_doubles(nmax));
+    if (kind == GIFT_XF_CHOL_TWO_SIDED) {
+      w.Gf = c.take<float>((size_t)d_out * d_out);
+      w.G64 = c.take<double>((size_t)d_out * d_out);
+      w.Gi64 = c.take<double>((size_t)d_out * d_out);
+    }
+  }
+  w.bytes = c.off;
+  return w;
+}
+
+#define CK(expr)                                   \
+  do {                                             \
+    if ((expr) != cudaSuccess) return GIFT_ERR_CUDA; \
+  } while (0)
+
+Launch mk(const gift_ctx *ctx, int *st, cudaStream_t s) {
+  Launch L;
+  L.stream = s;
+  L.sms = ctx->sms;
+  L.status = st;
+  return L;
+}
+
+gift_status check_factor(const gift_factor *f, int d_out, int d_in) {
+  if (!f || f->kind == GIFT_XF_IDENTITY) return GIFT_OK;
+  if (!valid_kind(f->kind)) return GIFT_ERR_INVALID_ARG;
+  if (f->d_in != d_in || f->d_out != d_out) return GIFT_ERR_INVALID_ARG;
+  if (f->kind == GIFT_XF_LOWRANK) {
+    if (!f->U || !f->mu || !f->sigma) return GIFT_ERR_INVALID_ARG;
+    if (f->rank < 1 || f->rank > kMaxRank || f->rank > d_in) return GIFT_ERR_INVALID_ARG;
+  } else {
+    if (!f->LA || !f->LAinv) return GIFT_ERR_INVALID_ARG;
+    if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!f->LG || !f->LGinv)) return GIFT_ERR_INVALID_ARG;
+  }
+  return GIFT_OK;
+}
+
+gift_xform kind_of(const gift_factor *f) { return f ? f->kind : GIFT_XF_IDENTITY; }
+
+// Full-rank transforms as GEMMs with the explicit inverses of the factor.
+cudaError_t chol_whiten(const Launch &L, const gift_factor *f, const float *W, int d_out, int d_in,
+                        const CodecWs &w) {
+  const float *src = W;
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
+    GemmArgs g{};
+    g.A = f->LGinv; g.B = W; g.C = w.tbuf;
+    g.M = d_out; g.N = d_in; g.K = d_out; g.lda = d_out; g.ldb = d_in; g.ldc = d_in;
+    g.a_lower = true; g.alpha = 1.0f;
+    cudaError_t e = launch_sgemm(L, g);
+    if (e != cudaSuccess) return e;
+    src = w.tbuf;
+  }
+  GemmArgs g{};
+  g.A = src; g.B = f->LAinv; g.C = w.xbuf;
+  g.M = d_out; g.N = d_in; g.K = d_in; g.lda = d_in; g.ldb = d_in; g.ldc = d_in;
+  g.transB = true; g.b_lower_t = true; g.alpha = 1.0f;
+  return launch_sgemm(L, g);
+}
+
+cudaError_t chol_unwhiten(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, float *out,
+                          const CodecWs &w) {
+  const float *src = X;
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
+    GemmArgs g{};
+    g.A = f->LG; g.B = X; g.C = w.tbuf;
+    g.M = d_out; g.N = d_in; g.K = d_out; g.lda = d_out; g.ldb = d_in; g.ldc = d_in;
+    g.a_lower = true; g.alpha = 1.0f;
+    cudaError_t e = launch_sgemm(L, g);
+    if (e != cudaSuccess) return e;
+    src = w.tbuf;
+  }
+  GemmArgs g{};
+  g.A = src; g.B = f->LA; g.C = out;
+  g.M = d_out; g.N = d_in; g.K = d_in; g.lda = d_in; g.ldb = d_in; g.ldc = d_in;
+  g.transB = true; g.b_lower_t = true; g.alpha = 1.0f;
+  return launch_sgemm(L, g);
+}
+
+LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w, bool inverse) {
+  LrApply a{};
+  a.X = X;
+  a.U = f->U;
+  a.Pc = w.Pc;
+  a.sigma = f->sigma;
+  a.rank = f->rank;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.inverse = inverse;
+  return a;
+}
+
+cudaError_t lr_prepare(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w,
+                       bool inverse) {
+  cudaError_t e = launch_lr_proj(L, X, d_out, d_in, f->U, f->rank, w.part, w.nsplit);
+  if (e != cudaSuccess) return e;
+  return launch_lr_finalize(L, w.part, w.nsplit, d_out, f->mu, f->sigma, f->rank, inverse, w.Pc);
+}
+
+}  // namespace
+
+// =========================================================================================
+extern "C" {
+
+gift_status gift_create(gift_ctx **ctx, int device) {
+  if (!ctx) return GIFT_ERR_INVALID_ARG;
+  *ctx = nullptr;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
+    return GIFT_ERR_CUDA;
+  gift_ctx *c = static_cast<gift_ctx *>(std::malloc(sizeof(gift_ctx)));
+  if (!c) return GIFT_ERR_CUDA;
+  c->device = device;
+  c->sms = sms;
+  c->subspace_iters = 10;
+  *ctx = c;
+  return GIFT_OK;
+}
+
+void gift_destroy(gift_ctx *ctx) { std::free(ctx); }
+
+gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value) {
+  if (!ctx) return GIFT_ERR_INVALID_ARG;
+  if (opt == GIFT_OPT_SUBSPACE_ITERS) {
+    if (value < 1 || value > 64) return GIFT_ERR_INVALID_ARG;
+    ctx->subspace_iters = (int)value;
+    return GIFT_OK;
+  }
+  return GIFT_ERR_INVALID_ARG;
+}
+
+const char *gift_status_string(gift_status s) {
+  switch (s) {
+    case GIFT_OK: return "ok";
+    case GIFT_ERR_INVALID_ARG: return "invalid argument";
+    case GIFT_ERR_UNSUPPORTED: return "unsupported combination";
+    case GIFT_ERR_CUDA: return "CUDA error";
+    case GIFT_ERR_NONFINITE: return "non-finite value in the tensor";
+    case GIFT_ERR_NOT_PD: return "factor is not positive definite";
+    case GIFT_ERR_TIMEOUT: return "bounded device wait timed out";
+    case GIFT_ERR_NOT_CONVERGED: return "eigensolver did not converge";
+  }
+  return "unknown status";
+}
+
+int gift_version(void) { return GIFT_VERSION_MAJOR * 1000 + GIFT_VERSION_MINOR; }
+
+size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gift_format fmt,
+                            gift_scaling scaling, int d_out, int d_in, int T, int rank) {
+  (void)T;
+  (void)rank;
+  if (!ctx || d_out <= 0 || d_in <= 0 || !valid_kind(kind) || !valid_fmt(fmt) || !valid_scaling(scaling))
+    return (size_t)-1;
+  if (op == GIFT_OP_FACTOR_UPDATE) {
+    if (kind == GIFT_XF_IDENTITY) return 0;
+    return factor_layout(nullptr, ctx->sms, kind, d_out, d_in).bytes;
+  }
+  if (op != GIFT_OP_ENCODE && op != GIFT_OP_DECODE && op != GIFT_OP_AMAX) return (size_t)-1;
+  return codec_layout(nullptr, ctx->sms, op, kind, d_out, d_in).bytes;
+}
+
+gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, int d_in, size_t *code_bytes,
+                            size_t *scale_count) {
+  if (!code_bytes || !scale_count || d_out <= 0 || d_in <= 0 || !valid_fmt(fmt) || !valid_scaling(scaling))
+    return GIFT_ERR_INVALID_ARG;
+  const size_t n = (size_t)d_out * d_in;
+  switch (fmt) {
+    case GIFT_FMT_F32:
+      *code_bytes = 4 * n;
+      *scale_count = 0;
+      break;
+    case GIFT_FMT_NVFP4:
+      if (d_in % kNvGroup) return GIFT_ERR_INVALID_ARG;
+      *code_bytes = n / 2;
+      *scale_count = n / kNvGroup;
+      break;
+    default:
+      *code_bytes = n;
+      *scale_count = (scaling == GIFT_SCALE_TENSOR)
+                         ? 1
+                         : (size_t)((d_out + kBlock - 1) / kBlock) * ((d_in + kBlock - 1) / kBlock);
+  }
+  return GIFT_OK;
+}
+
+// -----------------------------------------------------------------------------------------
+gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
+                               const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
+                               void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  (void)prec;
+  if (!ctx || !f || !a || T < 1) return GIFT_ERR_INVALID_ARG;
+  const int d_in = f->d_in, d_out = f->d_out;
+  if (d_in <= 0 || d_out <= 0) return GIFT_ERR_INVALID_ARG;
+  if (a_dt != GIFT_DT_F32 && a_dt != GIFT_DT_BF16) return GIFT_ERR_INVALID_ARG;
+  if (f->kind == GIFT_XF_IDENTITY || !valid_kind(f->kind)) return GIFT_ERR_INVALID_ARG;
+  gift_status cs = check_factor(f, d_out, d_in);
+  if (cs != GIFT_OK) return cs;
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!delta || (d_dt != GIFT_DT_F32 && d_dt != GIFT_DT_BF16)))
+    return GIFT_ERR_INVALID_ARG;
+  const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in);
+  const Launch L = mk(ctx, d_status, stream);
+
+  // A = a^T a / T (lower tiles, then mirrored)
+  auto syrk = [&](const void *x, bool bf16, int d, float *out) -> cudaError_t {
+    GemmArgs g{};
+    g.A = x; g.B = x; g.C = out;
+    g.M = d; g.N = d; g.K = T; g.lda = d; g.ldb = d; g.ldc = d;
+    g.transA = true; g.transB = false; g.a_bf16 = bf16; g.b_bf16 = bf16;
+    g.lower_tiles = true; g.alpha = 1.0f / (float)T;
+    cudaError_t e = launch_sgemm(L, g);
+    if (e != cudaSuccess) return e;
+    return launch_mirror_lower(L, out, d);
+  };
+  CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
+
+  if (f->kind == GIFT_XF_LOWRANK) {
+    const int k = w.k;
+    CK(launch_trace(L, w.A, d_in, w.tr));
+    auto cholqr = [&](const float *in, float *out) -> cudaError_t {
+      DgemmArgs g{};
+      g.A = in; g.B = in; g.C = w.Gp;
+      g.M = k; g.N = k; g.K = d_in; g.lda = k; g.ldb = k; g.ldc = k;
+      g.transA = true; g.transB = false; g.a_f32 = true; g.b_f32 = true;
+      g.alpha = 1.0; g.beta = 0.0; g.splits = w.gsplits; g.slice_stride = (size_t)k * k;
+      cudaError_t e = launch_dgemm(L, g);
+      if (e != cudaSuccess) return e;
+      if ((e = launch_sum_slices(L, w.Gp, w.gsplits, (size_t)k * k, (size_t)k * k, w.G, 1.0)) != cudaSuccess) return e;
+      if ((e = launch_small_chol_rinv(L, w.G, k, w.Rinv)) != cudaSuccess) return e;
+      DgemmArgs q{};
+      q.A = in; q.B = w.Rinv; q.C = w.Q64;
+      q.M = d_in; q.N = k; q.K = k; q.lda = k; q.ldb = k; q.ldc = k;
+      q.a_f32 = true; q.b_f32 = false; q.alpha = 1.0; q.beta = 0.0; q.splits = 1;
+      if ((e = launch_dgemm(L, q)) != cudaSuccess) return e;
+      return launch_f64_to_f32(L, w.Q64, out, (size_t)d_in * k, false, k);
+    };
+    auto aq = [&]() -> cudaError_t {   // Y = A Q
+      GemmArgs g{};
+      g.A = w.A; g.B = w.Q; g.C = w.Y;
+      g.M = d_in; g.N = k; g.K = d_in; g.lda = d_in; g.ldb = k; g.ldc = k; g.alpha = 1.0f;
+      return launch_sgemm_splitk(L, g, w.yparts, w.ysplits);
+    };
+    if (k == d_in) {
+      CK(launch_eye(L, w.Q, k));
+      CK(launch_f32_to_f64(L, w.A, w.G, (size_t)k * k));
+    } else {
+      CK(launch_philox_gaussian(L, w.Y, (size_t)d_in * k, seed));
+      CK(cholqr(w.Y, w.Q));
+      CK(cholqr(w.Q, w.Q));
+      for (int it = 0; it < ctx->subspace_iters; ++it) {
+        CK(aq());
+        CK(cholqr(w.Y, w.Q));
+        CK(cholqr(w.Q, w.Q));
+      }
+      CK(aq());
+      DgemmArgs g{};   // B = Q^T (A Q)
+      g.A = w.Q; g.B = w.Y; g.C = w.Gp;
+      g.M = k; g.N = k; g.K = d_in; g.lda = k; g.ldb = k; g.ldc = k;
+      g.transA = true; g.a_f32 = true; g.b_f32 = true;
+      g.alpha = 1.0; g.beta = 0.0; g.splits = w.gsplits; g.slice_stride = (size_t)k * k;
+      CK(launch_dgemm(L, g));
+      CK(launch_sum_slices(L, w.Gp, w.gsplits, (size_t)k * k, (size_t)k * k, w.G, 1.0));
+    }
+    CK(launch_jacobi(L, w.G, k, w.ev, w.V));
+    CK(launch_lowrank_outputs(L, w.Q, d_in, k, w.V, w.ev, w.tr, f->rank, f->U, f->mu, f->sigma));
+    return GIFT_OK;
+  }
+
+  // Cholesky variants
+  const size_t nn = (size_t)d_in * d_in;
+  CK(launch_f32_to_f64(L, w.A, w.A64, nn));
+  CK(launch_chol_inv(L, w.A64, w.Ai64, d_in, w.work));
+  CK(launch_f64_to_f32(L, w.A64, f->LA, nn, true, d_in));
+  CK(launch_f64_to_f32(L, w.Ai64, f->LAinv, nn, true, d_in));
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
+    const size_t mm = (size_t)d_out * d_out;
+    CK(syrk(delta, d_dt == GIFT_DT_BF16, d_out, w.Gf));
+    CK(launch_f32_to_f64(L, w.Gf, w.G64, mm));
+    CK(launch_chol_inv(L, w.G64, w.Gi64, d_out, w.work));
+    CK(launch_f64_to_f32(L, w.G64, f->LG, mm, true, d_out));
+    CK(launch_f64_to_f32(L, w.Gi64, f->LGinv, mm, true, d_out));
+  }
+  return GIFT_OK;
+}
+
+// -----------------------------------------------------------------------------------------
+static gift_status codec_common_checks(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
+                                       gift_format fmt, gift_scaling scaling) {
+  if (!ctx || !W || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt) || !valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && d_in % kNvGroup) return GIFT_ERR_INVALID_ARG;
+  return check_factor(f, d_out, d_in);
+}
+
+gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in, gift_format fmt,
+                      gift_scaling scaling, gift_precision prec, const float *residual, float *amax_accum, void *ws,
+                      size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  (void)prec;
+  gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
+  if (cs != GIFT_OK) return cs;
+  if (!amax_accum || fmt == GIFT_FMT_F32) return GIFT_ERR_INVALID_ARG;
+  const gift_xform kind = kind_of(f);
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
+  const Launch L = mk(ctx, d_status, stream);
+  const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
+  const size_t n = (size_t)d_out * d_in;
+  if (kind == GIFT_XF_LOWRANK) {
+    CK(lr_prepare(L, f, W, d_out, d_in, w, false));
+    LrApply a = lr_args(f, W, d_out, d_in, w, false);
+    a.R = const_cast<float *>(residual);   // read only by the amax epilogue
+    a.amax_ws = amax_accum;
+    CK(launch_lr_apply(L, block ? LR_BLOCK_AMAX : LR_AMAX, fmt, a));
+    return GIFT_OK;
+  }
+  const float *src = W;
+  if (kind != GIFT_XF_IDENTITY) {
+    CK(chol_whiten(L, f, W, d_out, d_in, w));
+    src = w.xbuf;
+  }
+  if (block) CK(launch_block128(L, fmt, 1, src, const_cast<float *>(residual), d_out, d_in, nullptr, nullptr,
+                                nullptr, amax_accum, nullptr, nullptr));
+  else CK(launch_amax(L, src, residual, n, amax_accum));
+  return GIFT_OK;
+}
+
+gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in, gift_format fmt,
+                        gift_scaling scaling, gift_precision prec, const float *amax_in, float *residual,
+                        void *codes, void *scales, float *tensor_scale, float *transformed_out, float *amax_out,
+                        void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  (void)prec;
+  gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
+  if (cs != GIFT_OK) return cs;
+  if (!codes) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && !tensor_scale) return GIFT_ERR_INVALID_ARG;
+  if (residual == W || (const void *)codes == (const void *)W) return GIFT_ERR_INVALID_ARG;
+  const gift_xform kind = kind_of(f);
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
+  const Launch L = mk(ctx, d_status, stream);
+  const size_t n = (size_t)d_out * d_in;
+  uint8_t *c8 = static_cast<uint8_t *>(codes);
+  const bool block = (scaling == GIFT_SCALE_BLOCK128);
+
+  if (kind == GIFT_XF_LOWRANK) {
+    CK(lr_prepare(L, f, W, d_out, d_in, w, false));
+    LrApply a = lr_args(f, W, d_out, d_in, w, false);
+    a.R = residual;
+    if (fmt == GIFT_FMT_F32) {
+      a.out = static_cast<float *>(codes);
+      CK(launch_lr_apply(L, LR_STORE, fmt, a));
+      if (transformed_out) CK(cudaMemcpyAsync(transformed_out, codes, n * 4, cudaMemcpyDeviceToDevice, stream));
+      if (residual) CK(cudaMemsetAsync(residual, 0, n * 4, stream));
+      return GIFT_OK;
+    }
+    a.tout = transformed_out;
+    a.codes = c8;
+    a.scales = scales;
+    a.tscale = tensor_scale;
+    a.amax_out = amax_out;
+    a.amax_in = amax_in;
+    if (fmt != GIFT_FMT_NVFP4 && block) {
+      CK(launch_lr_apply(L, LR_BLOCK, fmt, a));
+      return GIFT_OK;
+    }
+    if (!amax_in) {
+      CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
+      LrApply am = a;
+      am.tout = nullptr;
+      am.amax_ws = w.amax;
+      CK(launch_lr_apply(L, LR_AMAX, fmt, am));
+    }
+    a.amax_ws = w.amax;
+    CK(launch_lr_apply(L, fmt == GIFT_FMT_NVFP4 ? LR_NVFP4 : LR_PACK_TENSOR, fmt, a));
+    return GIFT_OK;
+  }
+
+  const float *src = W;
+  if (kind != GIFT_XF_IDENTITY) {
+    CK(chol_whiten(L, f, W, d_out, d_in, w));
+    src = w.xbuf;
+  }
+  if (fmt == GIFT_FMT_F32) {
+    CK(launch_pack_f32(L, src, residual, n, static_cast<float *>(codes), transformed_out));
+    return GIFT_OK;
+  }
+  if (fmt != GIFT_FMT_NVFP4 && block) {
+    CK(launch_block128(L, fmt, 0, src, residual, d_out, d_in, amax_in, c8, static_cast<float *>(scales), amax_out,
+                       transformed_out, nullptr));
+    return GIFT_OK;
+  }
+  const float *amax = amax_in;
+  if (!amax) {
+    CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
+    CK(launch_amax(L, src, residual, n, w.amax));
+    amax = w.amax;
+  }
+  if (fmt == GIFT_FMT_NVFP4)
+    CK(launch_pack_nvfp4(L, src, residual, n, amax, c8, static_cast<uint8_t *>(scales), tensor_scale, amax_out,
+                         transformed_out));
+  else
+    CK(launch_pack_tensor(L, fmt, src, residual, n, amax, c8, static_cast<float *>(scales), amax_out,
+                          transformed_out));
+  return GIFT_OK;
+}
+
+gift_status gift_replica_reduce(gift_ctx *ctx, int R, const void *const *codes, const void *const *scales,
+                                const float *const *tensor_scales, gift_format fmt, gift_scaling scaling, int d_out,
+                                int d_in, float *avg_out, int *d_status, cudaStream_t stream) {
+  if (!ctx || !codes || !avg_out || R < 1 || R > kMaxReplicas || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt) || !valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && (d_in % kNvGroup || !tensor_scales)) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
+  ReduceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < R; ++r) {
+    if (!codes[r]) return GIFT_ERR_INVALID_ARG;
+    a.codes[r] = codes[r];
+    if (fmt != GIFT_FMT_F32) {
+      if (!scales[r]) return GIFT_ERR_INVALID_ARG;
+      a.scales[r] = scales[r];
+    }
+    if (fmt == GIFT_FMT_NVFP4) {
+      if (!tensor_scales[r]) return GIFT_ERR_INVALID_ARG;
+      a.tscales[r] = tensor_scales[r];
+    }
+  }
+  const Launch L = mk(ctx, d_status, stream);
+  CK(launch_reduce(L, a, R, fmt, scaling, d_out, d_in, avg_out));
+  return GIFT_OK;
+}
+
+gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int in_is_codes, const void *scales,
+                        const float *tensor_scale, gift_format fmt, gift_scaling scaling, gift_precision prec,
+                        int d_out, int d_in, float *W_out, void *ws, size_t ws_bytes, int *d_status,
+                        cudaStream_t stream) {
+  (void)prec;
+  if (!ctx || !in || !W_out || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
+  if ((const void *)W_out == in) return GIFT_ERR_INVALID_ARG;
+  const bool codes_in = in_is_codes && fmt != GIFT_FMT_F32;
+  if (in_is_codes && (!valid_fmt(fmt) || !valid_scaling(scaling))) return GIFT_ERR_INVALID_ARG;
+  if (codes_in && !scales) return GIFT_ERR_INVALID_ARG;
+  if (codes_in && fmt == GIFT_FMT_NVFP4 && (d_in % kNvGroup || !tensor_scale)) return GIFT_ERR_INVALID_ARG;
+  gift_status cs = check_factor(f, d_out, d_in);
+  if (cs != GIFT_OK) return cs;
+  const gift_xform kind = kind_of(f);
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_DECODE, kind, d_out, d_in);
+  if (need.bytes && (!ws || ws_bytes < need.bytes)) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_DECODE, kind, d_out, d_in);
+  const Launch L = mk(ctx, d_status, stream);
+  const size_t n = (size_t)d_out * d_in;
+
+  // 1. the whitened tensor X in FP32
+  const float *X = static_cast<const float *>(in);
+  if (codes_in) {
+    float *dst = (kind == GIFT_XF_IDENTITY) ? W_out : w.xbuf;
+    ReduceArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.codes[0] = in;
+    a.scales[0] = scales;
+    a.tscales[0] = tensor_scale;
+    CK(launch_reduce(L, a, 1, fmt, scaling, d_out, d_in, dst));
+    if (kind == GIFT_XF_IDENTITY) return GIFT_OK;
+    X = w.xbuf;
+  }
+  // 2. map back
+  if (kind == GIFT_XF_IDENTITY) {
+    CK(launch_pack_f32(L, X, nullptr, n, W_out, nullptr));
+  } else if (kind == GIFT_XF_LOWRANK) {
+    CK(lr_prepare(L, f, X, d_out, d_in, w, true));
+    LrApply a = lr_args(f, X, d_out, d_in, w, true);
+    a.out = W_out;
+    CK(launch_lr_apply(L, LR_STORE, GIFT_FMT_F32, a));
+  } else {
+    CK(chol_unwhiten(L, f, X, d_out, d_in, W_out, w));
+  }
+  return GIFT_OK;
+}
+
+gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int d_in, gift_format fmt,
+                                   gift_scaling scaling, unsigned long long *d_counts, void *ws, size_t ws_bytes,
+                                   int *d_status, cudaStream_t stream) {
+  if (!ctx || !W || !d_counts || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_E4M3 && fmt != GIFT_FMT_E5M2) return GIFT_ERR_INVALID_ARG;
+  if (!valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
+  const Launch L = mk(ctx, d_status, stream);
+  if (scaling == GIFT_SCALE_BLOCK128) {
+    CK(launch_block128(L, fmt, 2, W, nullptr, d_out, d_in, nullptr, nullptr, nullptr, nullptr, nullptr, d_counts));
+    return GIFT_OK;
+  }
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, GIFT_XF_IDENTITY, d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_AMAX, GIFT_XF_IDENTITY, d_out, d_in);
+  const size_t n = (size_t)d_out * d_in;
+  CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
+  CK(launch_amax(L, W, nullptr, n, w.amax));
+  CK(launch_hits_tensor(L, fmt, W, n, w.amax, d_counts));
+  return GIFT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,261 @@
+"""Thin Python binding of libgift (ctypes).
+
+Every function here has the name of the C entry point it wraps and only marshals
+arguments: torch tensors become device pointers, None becomes NULL, the current
+torch stream becomes the cudaStream_t.  All arithmetic runs in libgift's CUDA
+kernels; nothing in this module computes on tensor data.  If libgift.so is not
+built, the first call raises RuntimeError (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgift.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "gift.h")
+
+# ---- enums (values fixed by include/gift.h) ---------------------------------------------
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NONFINITE, ERR_NOT_PD, ERR_TIMEOUT, ERR_NOT_CONVERGED = range(8)
+FMT = {"f32": 0, "e4m3": 1, "e5m2": 2, "nvfp4": 3}
+SCALING = {"tensor": 0, "block128": 1}
+XFORM = {"identity": 0, "lowrank": 1, "chol_input": 2, "chol_two_sided": 3}
+PREC = {"fp32": 0, "tc": 1}
+DTYPE = {"f32": 0, "bf16": 1}
+OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3}
+OPT_SUBSPACE_ITERS = 0
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+class GiftFactor(ctypes.Structure):
+    _fields_ = [("kind", _i), ("d_in", _i), ("d_out", _i), ("rank", _i),
+                ("U", _vp), ("mu", _vp), ("sigma", _vp),
+                ("LA", _vp), ("LAinv", _vp), ("LG", _vp), ("LGinv", _vp)]
+
+
+class GiftError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_LIB = None
+
+
+def _declare(lib):
+    sig = {
+        "gift_create": (_i, [ctypes.POINTER(_vp), _i]),
+        "gift_destroy": (None, [_vp]),
+        "gift_set_option": (_i, [_vp, _i, ctypes.c_longlong]),
+        "gift_status_string": (ctypes.c_char_p, [_i]),
+        "gift_version": (_i, []),
+        "gift_workspace_bytes": (_sz, [_vp, _i, _i, _i, _i, _i, _i, _i, _i]),
+        "gift_code_sizes": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
+        "gift_factor_update": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _vp, _i, ctypes.c_uint64, _i,
+                                    _vp, _sz, _vp, _vp]),
+        "gift_amax": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]),
+        "gift_encode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                             _vp, _vp, _sz, _vp, _vp]),
+        "gift_replica_reduce": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i, _i,
+                                     _i, _i, _vp, _vp, _vp]),
+        "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
+                             _vp, _vp]),
+        "gift_boundary_hit_rate": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+
+
+def lib():
+    """The loaded libgift (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libgift is not built ({LIB_PATH} missing); run fac_whitening_gb300.build.build()")
+        _LIB = ctypes.CDLL(LIB_PATH)
+        _declare(_LIB)
+    return _LIB
+
+
+def header_functions():
+    """Names of every function declared in include/gift.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_ ]+\*?\s*\*?(gift_[a-z0-9_]+)\s*\(", text, re.M)))
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise GiftError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib().gift_status_string(status).decode()
+
+
+def gift_version() -> int:
+    return lib().gift_version()
+
+
+# ---- context ------------------------------------------------------------------------------
+class Context:
+    """Owns one gift_ctx for a CUDA device."""
+
+    def __init__(self, device: int = 0):
+        h = _vp()
+        _check(lib().gift_create(ctypes.byref(h), device), "gift_create")
+        self.handle = h
+        self.device = device
+
+    def close(self):
+        if self.handle:
+            lib().gift_destroy(self.handle)
+            self.handle = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def gift_create(device: int = 0) -> Context:
+    return Context(device)
+
+
+def gift_set_option(ctx: Context, opt: int, value: int):
+    _check(lib().gift_set_option(ctx.handle, opt, value), "gift_set_option")
+
+
+def gift_workspace_bytes(ctx: Context, op: str, kind: str, fmt: str, scaling: str, d_out: int, d_in: int,
+                         T: int = 0, rank: int = 32) -> int:
+    n = lib().gift_workspace_bytes(ctx.handle, OP[op], XFORM[kind], FMT[fmt], SCALING[scaling], d_out, d_in, T, rank)
+    if n == ctypes.c_size_t(-1).value:
+        raise GiftError(ERR_INVALID_ARG, "gift_workspace_bytes")
+    return n
+
+
+def gift_code_sizes(fmt: str, scaling: str, d_out: int, d_in: int):
+    cb, sc = _sz(), _sz()
+    _check(lib().gift_code_sizes(FMT[fmt], SCALING[scaling], d_out, d_in, ctypes.byref(cb), ctypes.byref(sc)),
+           "gift_code_sizes")
+    return cb.value, sc.value
+
+
+# ---- factor -------------------------------------------------------------------------------
+@dataclass
+class Factor:
+    """Device buffers of one layer's factor (torch tensors owned by the caller)."""
+    kind: str
+    d_out: int
+    d_in: int
+    rank: int = 32
+    U: object = None
+    mu: object = None
+    sigma: object = None
+    LA: object = None
+    LAinv: object = None
+    LG: object = None
+    LGinv: object = None
+
+    @staticmethod
+    def empty(kind: str, d_out: int, d_in: int, rank: int = 32, device="cuda") -> "Factor":
+        import torch
+        f = Factor(kind, d_out, d_in, rank)
+        z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)  # noqa: E731
+        if kind == "lowrank":
+            f.U, f.mu, f.sigma = z(d_in, rank), z(rank), z(1)
+        elif kind in ("chol_input", "chol_two_sided"):
+            f.LA, f.LAinv = z(d_in, d_in), z(d_in, d_in)
+            if kind == "chol_two_sided":
+                f.LG, f.LGinv = z(d_out, d_out), z(d_out, d_out)
+        return f
+
+    def c_struct(self) -> GiftFactor:
+        return GiftFactor(XFORM[self.kind], self.d_in, self.d_out, self.rank, _p(self.U), _p(self.mu),
+                          _p(self.sigma), _p(self.LA), _p(self.LAinv), _p(self.LG), _p(self.LGinv))
+
+
+def _fptr(f: Optional[Factor]):
+    if f is None:
+        return None
+    return ctypes.byref(f.c_struct())
+
+
+def gift_factor_update(ctx: Context, f: Factor, a, delta=None, seed: int = 0, prec: str = "fp32", ws=None,
+                       status=None, stream=None):
+    import torch
+    a_dt = DTYPE["bf16"] if a.dtype == torch.bfloat16 else DTYPE["f32"]
+    d_dt = DTYPE["bf16"] if (delta is not None and delta.dtype == torch.bfloat16) else DTYPE["f32"]
+    st = f.c_struct()
+    _check(lib().gift_factor_update(ctx.handle, ctypes.byref(st), _p(a), a_dt, a.shape[0], _p(delta), d_dt,
+                                    seed, PREC[prec], _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                    _p(status), _stream(stream)), "gift_factor_update")
+
+
+def gift_amax(ctx: Context, f: Optional[Factor], W, fmt: str, scaling: str, amax_accum, residual=None,
+              prec: str = "fp32", ws=None, status=None, stream=None):
+    d_out, d_in = W.shape
+    _check(lib().gift_amax(ctx.handle, _fptr(f), _p(W), d_out, d_in, FMT[fmt], SCALING[scaling], PREC[prec],
+                           _p(residual), _p(amax_accum), _p(ws),
+                           0 if ws is None else ws.numel() * ws.element_size(), _p(status), _stream(stream)),
+           "gift_amax")
+
+
+def gift_encode(ctx: Context, f: Optional[Factor], W, fmt: str, scaling: str, codes, scales=None,
+                tensor_scale=None, amax_in=None, residual=None, transformed_out=None, amax_out=None,
+                prec: str = "fp32", ws=None, status=None, stream=None):
+    d_out, d_in = W.shape
+    _check(lib().gift_encode(ctx.handle, _fptr(f), _p(W), d_out, d_in, FMT[fmt], SCALING[scaling], PREC[prec],
+                             _p(amax_in), _p(residual), _p(codes), _p(scales), _p(tensor_scale),
+                             _p(transformed_out), _p(amax_out), _p(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _p(status), _stream(stream)),
+           "gift_encode")
+
+
+def gift_replica_reduce(ctx: Context, codes: Sequence, scales: Optional[Sequence], fmt: str, scaling: str,
+                        d_out: int, d_in: int, avg_out, tensor_scales: Optional[Sequence] = None, status=None,
+                        stream=None):
+    R = len(codes)
+    arr = lambda xs: (_vp * R)(*[_p(x) for x in xs]) if xs is not None else None  # noqa: E731
+    _check(lib().gift_replica_reduce(ctx.handle, R, arr(codes), arr(scales), arr(tensor_scales), FMT[fmt],
+                                     SCALING[scaling], d_out, d_in, _p(avg_out), _p(status), _stream(stream)),
+           "gift_replica_reduce")
+
+
+def gift_decode(ctx: Context, f: Optional[Factor], inp, in_is_codes: bool, fmt: str, scaling: str, d_out: int,
+                d_in: int, W_out, scales=None, tensor_scale=None, prec: str = "fp32", ws=None, status=None,
+                stream=None):
+    _check(lib().gift_decode(ctx.handle, _fptr(f), _p(inp), int(bool(in_is_codes)), _p(scales), _p(tensor_scale),
+                             FMT[fmt], SCALING[scaling], PREC[prec], d_out, d_in, _p(W_out), _p(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _p(status), _stream(stream)),
+           "gift_decode")
+
+
+def gift_boundary_hit_rate(ctx: Context, W, fmt: str, scaling: str, counts, ws=None, status=None, stream=None):
+    d_out, d_in = W.shape
+    _check(lib().gift_boundary_hit_rate(ctx.handle, _p(W), d_out, d_in, FMT[fmt], SCALING[scaling], _p(counts),
+                                        _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                        _stream(stream)), "gift_boundary_hit_rate")

@@ -1,0 +1,43 @@
+"""The C ABI library loads on a CPU-only machine and exports every declared function."""
+import ctypes
+
+import pytest
+
+from fac_whitening_gb300 import gift as G
+
+
+def _lib_or_skip():
+    try:
+        return G.lib()
+    except RuntimeError as e:  # not built in this checkout
+        pytest.skip(str(e))
+
+
+def test_exports_every_declared_function():
+    lib = _lib_or_skip()
+    names = G.header_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_host_only_helpers():
+    _lib_or_skip()
+    assert G.gift_version() == 1
+    assert G.status_string(G.OK) == "ok"
+    assert G.status_string(G.ERR_NOT_PD).startswith("factor")
+    assert G.gift_code_sizes("e4m3", "tensor", 10, 20) == (200, 1)
+    assert G.gift_code_sizes("e5m2", "block128", 300, 200) == (60000, 6)
+    assert G.gift_code_sizes("nvfp4", "tensor", 4, 32) == (64, 8)
+    assert G.gift_code_sizes("f32", "tensor", 3, 5) == (60, 0)
+    with pytest.raises(G.GiftError):
+        G.gift_code_sizes("nvfp4", "tensor", 4, 30)   # d_in not a multiple of 16
+    with pytest.raises(G.GiftError):
+        G.gift_code_sizes("e4m3", "tensor", 0, 5)
+
+
+def test_null_context_is_rejected():
+    lib = _lib_or_skip()
+    assert lib.gift_create(None, 0) == G.ERR_INVALID_ARG
+    assert lib.gift_set_option(None, 0, 10) == G.ERR_INVALID_ARG
+    assert lib.gift_workspace_bytes(None, 1, 0, 1, 0, 4, 4, 0, 0) == ctypes.c_size_t(-1).value

@@ -1,0 +1,113 @@
+"""GPU factor refresh against the oracle: K-FAC factor (eq. (4)), rank-r eigenpairs
+(eq. (17), eigenvalues within 1e-3 relative over the top 32) and the Cholesky
+factors (eq. (7): L L^T = A, L^-1 A L^-T = I)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fac_whitening_gb300 import gift as G
+from fac_whitening_gb300 import synth
+
+from gpu_util import DEV, ctx, rel_fro, status, t
+
+pytestmark = pytest.mark.gpu
+
+
+def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None):
+    d_in = a.shape[1]
+    f = G.Factor.empty(kind, d_out, d_in, rank)
+    n = G.gift_workspace_bytes(ctx(), "factor_update", kind, "e4m3", "tensor", d_out, d_in, a.shape[0], rank)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    st = status()
+    if iters:
+        G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, iters)
+    G.gift_factor_update(ctx(), f, a, delta=delta, seed=seed, ws=w, status=st)
+    torch.cuda.synchronize()
+    if iters:
+        G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, 10)
+    return f, w, int(st.item())
+
+
+def check_lowrank(f, a64, rank, st):
+    assert st == 0
+    A = O.kfac_factor(a64)
+    ev = np.sort(np.linalg.eigvalsh(A))[::-1]
+    mu = f.mu.cpu().double().numpy()
+    U = f.U.cpu().double().numpy()
+    np.testing.assert_allclose(mu, ev[:rank], rtol=1e-3)
+    d = A.shape[0]
+    sigma = float(f.sigma.item())
+    want_sigma = 1.0 if rank == d else (np.trace(A) - ev[:rank].sum()) / (d - rank)
+    assert abs(sigma - want_sigma) <= 1e-3 * abs(want_sigma)
+    np.testing.assert_allclose(U.T @ U, np.eye(rank), atol=1e-5)
+    # residual bound: some exact eigenvalue lies within ||A u - mu u|| of mu
+    res = np.linalg.norm(A @ U - U * mu, axis=0)
+    assert np.all(res <= 1e-3 * mu), res / mu
+    # against the oracle's own factor
+    Fo = O.lowrank_factor_from_activations(a64, r=rank)
+    np.testing.assert_allclose(mu, Fo.mu, rtol=1e-3)
+
+
+def test_factor_lowrank_tiny():
+    spec = synth.tiny_workload().layers[0]
+    _, a = synth.layer_inputs(spec, 0, 0, 1)
+    f, w, st = run_factor("lowrank", t(a), 64)
+    check_lowrank(f, a.double().numpy(), 32, st)
+    # the SYRK result sits at the start of the workspace: A = a^T a / T
+    A_gpu = w[: 256 * 256 * 4].view(torch.float32).view(256, 256).cpu().double().numpy()
+    assert rel_fro(A_gpu, O.kfac_factor(a.double().numpy())) <= 1e-6
+
+
+def test_factor_lowrank_bf16_steep():
+    spec = synth.LayerSpec("m", 128, 1024, T=4096, exponent=1.2, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
+    f, _, st = run_factor("lowrank", a, 128)
+    check_lowrank(f, a.double().cpu().numpy(), 32, st)
+
+
+def test_factor_exact_rank_equals_d_in():
+    rng = np.random.default_rng(5)
+    a = (rng.standard_normal((200, 16)) * np.linspace(2, 0.3, 16)).astype(np.float32)
+    f, _, st = run_factor("lowrank", t(a), 8, rank=16)
+    check_lowrank(f, a.astype(np.float64), 16, st)
+    F = O.LowRankFactor(f.U.cpu().double().numpy(), f.mu.cpu().double().numpy(), f.sigma.item())
+    T = O.lowrank_T(F)
+    A = O.kfac_factor(a.astype(np.float64))
+    np.testing.assert_allclose(T.T @ A @ T, np.eye(16), atol=1e-4)
+
+
+@pytest.mark.parametrize("kind", ["chol_input", "chol_two_sided"])
+def test_factor_cholesky(kind):
+    spec = synth.LayerSpec("c", 96, 320, T=2048, exponent=0.5, act_dtype=torch.float32)
+    _, a = synth.layer_inputs(spec, 9, 4, 1)
+    delta = synth.delta_for_layer(spec, 9, 4)
+    f, _, st = run_factor(kind, t(a), 96, delta=t(delta) if kind == "chol_two_sided" else None)
+    assert st == 0
+    pairs = [(f.LA, f.LAinv, a)]
+    if kind == "chol_two_sided":
+        pairs.append((f.LG, f.LGinv, delta))
+    for Lt, Lit, x in pairs:
+        A = O.kfac_factor(x.double().numpy())
+        L = Lt.cpu().double().numpy()
+        Li = Lit.cpu().double().numpy()
+        assert np.all(np.triu(L, 1) == 0) and np.all(np.triu(Li, 1) == 0)
+        assert rel_fro(L @ L.T, A) <= 1e-6
+        np.testing.assert_allclose(Li @ A @ Li.T, np.eye(A.shape[0]), atol=1e-4)
+        assert rel_fro(L, O.cholesky(A)) <= 1e-4
+
+
+def test_factor_cholesky_not_pd_status():
+    a = np.zeros((64, 80), np.float32)           # A = 0: the first pivot is not positive
+    f, _, st = run_factor("chol_input", t(a), 8)
+    assert st == G.ERR_NOT_PD
+
+
+def test_philox_start_is_seeded():
+    spec = synth.tiny_workload().layers[0]
+    _, a = synth.layer_inputs(spec, 0, 1, 1)
+    f1, _, _ = run_factor("lowrank", t(a), 64, seed=1)
+    f2, _, _ = run_factor("lowrank", t(a), 64, seed=1)
+    f3, _, _ = run_factor("lowrank", t(a), 64, seed=2)
+    assert torch.equal(f1.U, f2.U) and torch.equal(f1.mu, f2.mu)
+    np.testing.assert_allclose(f1.mu.cpu().numpy(), f3.mu.cpu().numpy(), rtol=1e-4)

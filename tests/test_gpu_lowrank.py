@@ -1,0 +1,145 @@
+"""GPU parity of the rank-r whitening codec (simplification 2, eq. (17)) against the oracle.
+
+The factor (U, mu, sigma) is the oracle's, rounded to FP32 and given to both sides.
+Transforms and decoded tensors: relative Frobenius error <= 1e-5 (FP32 path).
+Codes: bit-exact when the oracle quantises the GPU's transformed tensor; against
+the oracle's own transformed tensor, codes may differ only where the two FP32
+values straddle a rounding boundary (by one code step, on a tiny fraction)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fac_whitening_gb300 import gift as G
+from fac_whitening_gb300 import synth
+
+from gpu_util import DEV, ctx, encode, factor_to_gpu, rel_fro, status, t, ws
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-5
+
+
+def make_layer(d_out, d_in, T, exponent, seed, rank=32, R=1, dtype=torch.float32, device="cpu"):
+    spec = synth.LayerSpec("t", d_out, d_in, T=T, exponent=exponent, act_dtype=dtype)
+    Ws, a = synth.layer_inputs(spec, 9, seed, R, device=device)
+    a64 = a.to(torch.float64).cpu().numpy()
+    F = O.lowrank_factor_from_activations(a64, r=rank)
+    F32 = O.LowRankFactor(F.U.astype(np.float32), F.mu.astype(np.float32), np.float32(F.sigma))
+    return [W.cpu().numpy() for W in Ws], F32, a
+
+
+def oracle_codes_close(got, want, fmt):
+    """Codes of two nearly equal tensors: equal, or one code step apart on few elements."""
+    diff = got != want
+    frac = np.count_nonzero(diff) / diff.size
+    assert frac < 2e-3, frac
+    if fmt in ("e4m3", "e5m2"):
+        f = O.FORMATS[fmt]
+        vg, vw = O.decode(got[diff], f), O.decode(want[diff], f)
+        step = np.abs(vw) * 2.0 ** -f.mbits + f.min_subnormal
+        assert np.all(np.abs(vg - vw) <= step * 1.0001)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return make_layer(64, 256, 512, 1.0, 0, R=4)
+
+
+@pytest.fixture(scope="module")
+def c3():
+    # a 600M-like fc2 layer, 1536 x 6144, with the factor from 4096 tokens
+    return make_layer(1536, 6144, 4096, 1.2, 1, R=1, dtype=torch.bfloat16, device="cuda")
+
+
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "tensor"), ("e4m3", "block128"),
+                                         ("nvfp4", "tensor")])
+@pytest.mark.parametrize("which", ["tiny", "c3"])
+def test_lowrank_encode(which, fmt, scaling, request):
+    Ws, F, _ = request.getfixturevalue(which)
+    W = Ws[0]
+    f = factor_to_gpu("lowrank", *W.shape, F=F)
+    out = encode(f, W, fmt, scaling)
+    assert out["status"] == 0
+    want = O.lowrank_whiten(W, F)
+    assert rel_fro(out["tout"], want) <= TOL
+    qg = O.quantize(out["tout"], fmt, scaling)                 # the quantiser contract, bit-exact
+    np.testing.assert_array_equal(out["codes"], qg["codes"])
+    np.testing.assert_array_equal(out["scales"], qg["scales"])
+    qo = O.quantize(want.astype(np.float32), fmt, scaling)     # against the oracle's own transform
+    oracle_codes_close(out["codes"], qo["codes"], fmt)
+
+
+def test_lowrank_error_feedback(tiny):
+    Ws, F, _ = tiny
+    W = Ws[1]
+    R0 = (0.01 * np.random.default_rng(2).standard_normal(W.shape)).astype(np.float32)
+    f = factor_to_gpu("lowrank", *W.shape, F=F)
+    out = encode(f, W, "e4m3", residual=R0)
+    Ut = out["tout"]
+    assert rel_fro(Ut, (O.lowrank_whiten(W, F) + R0)) <= TOL
+    q = O.quantize(Ut, "e4m3")
+    np.testing.assert_array_equal(out["codes"], q["codes"])
+    np.testing.assert_array_equal(out["residual"], (Ut - O.dequantize_any(q, "e4m3")).astype(np.float32))
+
+
+@pytest.mark.parametrize("which", ["tiny", "c3"])
+def test_lowrank_decode_and_roundtrip(which, request):
+    Ws, F, _ = request.getfixturevalue(which)
+    W = Ws[0]
+    d_out, d_in = W.shape
+    f = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    X = np.random.default_rng(3).standard_normal(W.shape).astype(np.float32)
+    Wo = torch.empty(d_out, d_in, dtype=torch.float32, device=DEV)
+    st = status()
+    w = ws("decode", "lowrank", "f32", "tensor", d_out, d_in)
+    G.gift_decode(ctx(), f, t(X), False, "f32", "tensor", d_out, d_in, Wo, ws=w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert rel_fro(Wo.cpu().numpy(), O.lowrank_unwhiten(X, F)) <= TOL
+    # lossless format: map back inverts the whitening (common confusions: lossless GIFT == baseline)
+    enc = encode(f, W, "f32")
+    G.gift_decode(ctx(), f, enc["_dev"][0], False, "f32", "tensor", d_out, d_in, Wo, ws=w)
+    torch.cuda.synchronize()
+    assert rel_fro(Wo.cpu().numpy(), W) <= TOL
+    # decode straight from codes = dequantise then map back
+    e8 = encode(f, W, "e4m3")
+    G.gift_decode(ctx(), f, e8["_dev"][0], True, "e4m3", "tensor", d_out, d_in, Wo, scales=e8["_dev"][1], ws=w)
+    torch.cuda.synchronize()
+    deq = O.dequantize_any(O.quantize(e8["tout"], "e4m3"), "e4m3")
+    assert rel_fro(Wo.cpu().numpy(), O.lowrank_unwhiten(deq, F)) <= TOL
+
+
+def test_lowrank_reduce_decode_pipeline(tiny):
+    Ws, F, _ = tiny
+    d_out, d_in = Ws[0].shape
+    f = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    outs = [encode(f, W, "e4m3") for W in Ws]
+    avg = torch.empty(d_out, d_in, dtype=torch.float32, device=DEV)
+    G.gift_replica_reduce(ctx(), [o["_dev"][0] for o in outs], [o["_dev"][1] for o in outs], "e4m3", "tensor",
+                          d_out, d_in, avg)
+    torch.cuda.synchronize()
+    qs = [O.quantize(o["tout"], "e4m3") for o in outs]
+    np.testing.assert_array_equal(avg.cpu().numpy(), O.replica_reduce(qs, "e4m3"))
+
+
+@pytest.mark.parametrize("rank,d_in", [(8, 256), (16, 16), (1, 40)])
+def test_lowrank_small_ranks(rank, d_in):
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal((300, d_in)) * np.linspace(3, 0.2, d_in)
+    F = O.lowrank_factor_from_A(O.kfac_factor(a), r=rank)
+    F = O.LowRankFactor(F.U.astype(np.float32), F.mu.astype(np.float32), np.float32(F.sigma))
+    W = rng.standard_normal((50, d_in)).astype(np.float32)
+    f = factor_to_gpu("lowrank", 50, d_in, F=F)
+    out = encode(f, W, "e4m3")
+    assert rel_fro(out["tout"], O.lowrank_whiten(W, F)) <= TOL
+    np.testing.assert_array_equal(out["codes"], O.quantize(out["tout"], "e4m3")["codes"])
+
+
+def test_lowrank_amax_matches_transformed(tiny):
+    Ws, F, _ = tiny
+    f = factor_to_gpu("lowrank", *Ws[0].shape, F=F)
+    acc = torch.zeros(1, dtype=torch.float32, device=DEV)
+    G.gift_amax(ctx(), f, t(Ws[2]), "e4m3", "tensor", acc, ws=ws("amax", "lowrank", "e4m3", "tensor", *Ws[2].shape))
+    torch.cuda.synchronize()
+    out = encode(f, Ws[2], "e4m3")
+    assert acc.item() == np.max(np.abs(out["tout"])) == out["amax"][0]
