@@ -114,8 +114,9 @@ cudaError_t launch_eye(const Launch &L, float *Q, int n) {
 // =====================================================================================
 __global__ void __launch_bounds__(256) k_small_chol_rinv(const double *__restrict__ G, int k,
                                                          double *__restrict__ Rinv) {
-  __shared__ double S[64][65];
-  __shared__ double X[64][65];
+  extern __shared__ double qr_sm[];   // two 64 x 65 tiles, opt-in size
+  double(*S)[65] = reinterpret_cast<double(*)[65]>(qr_sm);
+  double(*X)[65] = reinterpret_cast<double(*)[65]>(qr_sm + 64 * 65);
   const int tid = threadIdx.x;
   for (int idx = tid; idx < k * k; idx += 256) S[idx / k][idx % k] = G[idx];
   __syncthreads();
@@ -159,7 +160,10 @@ __global__ void __launch_bounds__(256) k_small_chol_rinv(const double *__restric
 }
 
 cudaError_t launch_small_chol_rinv(const Launch &L, const double *G, int k, double *Rinv) {
-  k_small_chol_rinv<<<1, 256, 0, L.stream>>>(G, k, Rinv);
+  const int smem = 2 * 64 * 65 * (int)sizeof(double);
+  cudaError_t e = cudaFuncSetAttribute(k_small_chol_rinv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_small_chol_rinv<<<1, 256, smem, L.stream>>>(G, k, Rinv);
   return cudaGetLastError();
 }
 

@@ -382,8 +382,9 @@ constexpr int kCholBase = 64;
 // One CTA: factor the n x n (n <= 64) block at A (leading dimension lda) in place into L
 // (upper part zeroed) and write L^-1 (lower, upper zeroed) at Li (leading dimension ldl).
 __global__ void __launch_bounds__(256) k_chol_inv_small(double *A, int lda, double *Li, int ldl, int n, int *status) {
-  __shared__ double S[kCholBase][kCholBase + 1];
-  __shared__ double X[kCholBase][kCholBase + 1];
+  extern __shared__ double chol_sm[];   // two (kCholBase x kCholBase+1) tiles, opt-in size
+  double(*S)[kCholBase + 1] = reinterpret_cast<double(*)[kCholBase + 1]>(chol_sm);
+  double(*X)[kCholBase + 1] = reinterpret_cast<double(*)[kCholBase + 1]>(chol_sm + kCholBase * (kCholBase + 1));
   __shared__ int bad;
   const int tid = threadIdx.x;
   if (tid == 0) bad = 0;
@@ -466,7 +467,10 @@ static cudaError_t chol_inv_rec(const Launch &L, double *A, double *Li, int ld, 
   double *Ab = A + (size_t)o * ld + o;
   double *Lb = Li + (size_t)o * ld + o;
   if (n <= kCholBase) {
-    k_chol_inv_small<<<1, 256, 0, L.stream>>>(Ab, ld, Lb, ld, n, L.status);
+    const int smem = 2 * kCholBase * (kCholBase + 1) * (int)sizeof(double);
+    cudaError_t e0 = cudaFuncSetAttribute(k_chol_inv_small, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e0 != cudaSuccess) return e0;
+    k_chol_inv_small<<<1, 256, smem, L.stream>>>(Ab, ld, Lb, ld, n, L.status);
     return cudaGetLastError();
   }
   int n1 = ((n / 2 + kCholBase - 1) / kCholBase) * kCholBase;
