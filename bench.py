@@ -1,0 +1,451 @@
+"""Benchmark of the GIFT gradient codec (libgift) on the 600M-like selective workload.
+
+One step = one pass of the codec over one batch of synthetic gradients of the
+Llama-600M-like selective deployment: 13 fc2 layers (1536 x 6144) take the
+geometry-aware branch (rank-32 input-side whitening, E4M3 per-tensor local scale)
+and 60 Euclidean tensors (1536 x 1536 / 1536 x 6144) take the Euclidean path
+(AllReduceMax'd shared scale), each over R = 8 replica gradients held in HBM:
+  geometry-aware layer: 8 x gift_encode -> gift_replica_reduce -> gift_decode
+  Euclidean tensor:     8 x gift_amax   -> 8 x gift_encode(shared amax) -> gift_replica_reduce
+The factor refresh (gift_factor_update on each layer's activations, T = 16384 BF16)
+runs every K = 50 steps in the method and is timed separately.
+
+value = FP32 gradient bytes entering the codec per step (sum over tensors of
+R * 4 * d_out * d_in) / step time, in GB/s, device-resident inputs, inputs larger
+than L2 (so no flush is needed).  Each stage group is captured in its own CUDA graph;
+a step replays the six graphs on one stream and CUDA events between them give each
+group's time inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gift|reference]
+With N > 1 (under torch.distributed.run) every rank runs the same per-GPU workload
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GIFT encode+decode GB/s of FP32 gradient and % HBM roofline, 600M-like fc2"
+UNIT = "GB/s"
+FMT = "e4m3"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="gift", choices=["gift", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=13, help="geometry-aware layers (13 in the workload)")
+    p.add_argument("--euclid", type=int, default=30, help="Euclidean tensors of each shape (30 in the workload)")
+    return p.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+# --------------------------------------------------------------------------------------
+def oracle_sample_step(sample):
+    import oracle as O
+    W_g, W_e, F = sample["gift"], sample["euclid"], sample["factor"]
+    xf = O.Xform("lowrank", F=F)
+    qs = [O.encode_layer(W, xf, FMT)[0] for W in W_g]
+    X = O.replica_reduce(qs, FMT)
+    O.decode_layer(X, xf)
+    shared = max(O.abs_max(W) for W in W_e)
+    qe = [O.quantize(W, FMT, amax=shared) for W in W_e]
+    O.replica_reduce(qe, FMT)
+
+
+def make_oracle_sample(rows=192, R=8):
+    """One geometry-aware layer and one Euclidean tensor, `rows` x 6144, R replicas (CPU)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from fac_whitening_gb300 import synth
+    spec = synth.LayerSpec("sample", rows, 6144, T=2048, exponent=1.0)
+    Ws, a = synth.layer_inputs(spec, 2, 77, R, device="cpu")
+    F = O.lowrank_factor_from_activations(a.to(torch.float64).numpy(), r=32, iters=8)
+    We = [synth.gaussian((rows, 6144), synth.seed_for(2, 99, r)).numpy() for r in range(R)]
+    nbytes = 2 * R * rows * 6144 * 4
+    return {"gift": [W.numpy() for W in Ws], "euclid": We, "factor": F, "bytes": nbytes,
+            "desc": f"one 1536x6144 fc2 layer and one Euclidean 1536x6144 tensor, first {rows} rows, R={R}"}
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    sample = make_oracle_sample()
+    for _ in range(args.warmup):
+        oracle_sample_step(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(sample)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sample["bytes"] / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32", "data": "synthetic",
+            "config": {"workload": "llama600m-selective (oracle sample)", "sample": sample["desc"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample["desc"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def build_workload(args, dev):
+    import torch
+    from fac_whitening_gb300 import synth
+    wl = synth.llama600m_selective_workload(seed_layers=args.layers, euclid_each=args.euclid)
+    R = wl.R
+    gift_layers, euclid = [], []
+    for li, spec in enumerate(wl.layers):
+        if spec.kind == "gift":
+            Ws, a = synth.layer_inputs(spec, wl.config, li, R, device=dev)
+            gift_layers.append({"spec": spec, "W": Ws, "a": a})
+        else:
+            Ws, _ = synth.layer_inputs(spec, wl.config, li, R, device=dev)
+            euclid.append({"spec": spec, "W": Ws})
+    torch.cuda.synchronize()
+    return wl, gift_layers, euclid
+
+
+def main_gift(args):
+    import numpy as np
+    import torch
+
+    from fac_whitening_gb300 import gift as G
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    ctx = G.Context(local)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+
+    wl, gl, eu = build_workload(args, dev)
+    R = wl.R
+    stream = torch.cuda.current_stream()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # ---- factor refresh (timed separately) -------------------------------------------
+    d_out, d_in = 1536, 6144
+    T = gl[0]["a"].shape[0] if gl else 0
+    fws = torch.zeros(G.gift_workspace_bytes(ctx, "factor_update", "lowrank", FMT, "tensor", d_out, d_in, T),
+                      dtype=torch.uint8, device=dev)
+    factors = []
+    fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i, L in enumerate(gl):   # warm-up refresh of the first layer
+        f = G.Factor.empty("lowrank", d_out, d_in, 32, device=dev)
+        factors.append(f)
+    if gl:
+        G.gift_factor_update(ctx, factors[0], gl[0]["a"], seed=1, ws=fws, status=st)
+    torch.cuda.synchronize()
+    fe0.record()
+    for i, L in enumerate(gl):
+        G.gift_factor_update(ctx, factors[i], L["a"], seed=1000 + i, ws=fws, status=st)
+    fe1.record()
+    torch.cuda.synchronize()
+    factor_ms = fe0.elapsed_time(fe1) / max(len(gl), 1)
+    syrk_flops = float(d_in) * d_in * T        # a^T a over T tokens (both triangles counted once)
+    for L in gl:
+        del L["a"]
+    torch.cuda.empty_cache()
+
+    # ---- buffers -----------------------------------------------------------------------
+    ws_bytes = max(G.gift_workspace_bytes(ctx, op, k, FMT, "tensor", d_out, d_in)
+                   for op in ("encode", "decode", "amax") for k in ("lowrank", "identity"))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def codes_for(spec):
+        return ([torch.empty(spec.d_out * spec.d_in, dtype=torch.uint8, device=dev) for _ in range(R)],
+                [torch.empty(1, dtype=torch.float32, device=dev) for _ in range(R)])
+
+    for L in gl:
+        L["codes"], L["scales"] = codes_for(L["spec"])
+        L["avg"] = torch.empty(d_out, d_in, dtype=torch.float32, device=dev)
+        L["out"] = torch.empty(d_out, d_in, dtype=torch.float32, device=dev)
+    shared = torch.zeros(max(len(eu), 1), dtype=torch.float32, device=dev)
+    for j, E in enumerate(eu):
+        E["codes"], E["scales"] = codes_for(E["spec"])
+        E["avg"] = torch.empty(E["spec"].d_out, E["spec"].d_in, dtype=torch.float32, device=dev)
+        E["shared"] = shared[j:j + 1]
+
+    # ---- stage groups ------------------------------------------------------------------
+    def g_encode():
+        for f, L in zip(factors, gl):
+            for r in range(R):
+                G.gift_encode(ctx, f, L["W"][r], FMT, "tensor", L["codes"][r], L["scales"][r], ws=ws, status=st)
+
+    def g_reduce():
+        for L in gl:
+            G.gift_replica_reduce(ctx, L["codes"], L["scales"], FMT, "tensor", d_out, d_in, L["avg"], status=st)
+
+    def g_decode():
+        for f, L in zip(factors, gl):
+            G.gift_decode(ctx, f, L["avg"], False, "f32", "tensor", d_out, d_in, L["out"], ws=ws, status=st)
+
+    def e_amax():
+        shared.zero_()
+        for E in eu:
+            for r in range(R):
+                G.gift_amax(ctx, None, E["W"][r], FMT, "tensor", E["shared"], ws=ws, status=st)
+
+    def e_encode():
+        for E in eu:
+            for r in range(R):
+                G.gift_encode(ctx, None, E["W"][r], FMT, "tensor", E["codes"][r], E["scales"][r],
+                              amax_in=E["shared"], ws=ws, status=st)
+
+    def e_reduce():
+        for E in eu:
+            s = E["spec"]
+            G.gift_replica_reduce(ctx, E["codes"], E["scales"], FMT, "tensor", s.d_out, s.d_in, E["avg"], status=st)
+
+    groups = [("gift_encode", g_encode), ("gift_reduce", g_reduce), ("gift_decode", g_decode),
+              ("euclid_amax", e_amax), ("euclid_encode", e_encode), ("euclid_reduce", e_reduce)]
+    n_gift = len(gl) * d_out * d_in
+    n_eu = sum(E["spec"].d_out * E["spec"].d_in for E in eu)
+    # algorithmic bytes and launches of each group (per step)
+    alg = {"gift_encode": (R * n_gift * 5, len(gl) * R * 4, len(gl) * R),
+           "gift_reduce": (n_gift * (R + 4), len(gl), len(gl)),
+           "gift_decode": (n_gift * 8, len(gl) * 3, len(gl)),
+           "euclid_amax": (R * n_eu * 4, len(eu) * R, len(eu) * R),
+           "euclid_encode": (R * n_eu * 5, len(eu) * R, len(eu) * R),
+           "euclid_reduce": (n_eu * (R + 4), len(eu), len(eu))}
+    kernels_per_step = sum(v[1] for v in alg.values())
+    grad_bytes = R * 4 * (n_gift + n_eu)
+
+    # eager warm-up (also loads every kernel), then capture one graph per group
+    for _, fn in groups:
+        fn()
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream()
+    with torch.cuda.stream(cap):
+        for name, fn in groups:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+            graphs.append((name, g))
+    torch.cuda.synchronize()
+
+    def step(evs=None):
+        for i, (name, g) in enumerate(graphs):
+            g.replay()
+            if evs is not None:
+                evs[i + 1].record()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st.zero_()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for k in range(args.steps):
+            ev[k][0].record()
+            step(ev[k])
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms = total_ms / args.steps
+    status_word = int(st.item())
+    group_ms = {name: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+                for i, (name, _) in enumerate(graphs)}
+    value = world * grad_bytes / (ms * 1e-3) / 1e9
+
+    # dominant group: the largest share of the step
+    dom = max(group_ms, key=group_ms.get)
+    bytes_g, launches_g, calls_g = alg[dom]
+    per_call_ms = group_ms[dom] / calls_g
+    achieved = bytes_g / calls_g / (per_call_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("group") == dom:
+            traffic = tj.get("bytes_per_call")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic, "kernel": dom,
+                "peak_kind": peak_kind, "per_call_us": per_call_ms * 1e3,
+                "algorithmic_bytes_per_call": bytes_g / calls_g}
+    stages = {name: {"ms": group_ms[name], "share": group_ms[name] / sum(group_ms.values()),
+                     "GB/s_algorithmic": alg[name][0] / (group_ms[name] * 1e-3) / 1e9,
+                     "hbm_frac": alg[name][0] / (group_ms[name] * 1e-3) / 1e9 / hbm_peak}
+              for name in group_ms}
+
+    # ---- end to end through the public API with host buffers --------------------------
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes)
+
+    # ---- CPU baseline (oracle on a bounded sample) --------------------------------------
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        sample = make_oracle_sample()
+        t_a = time.perf_counter()
+        oracle_sample_step(sample)
+        dt = time.perf_counter() - t_a
+        cpu = {"value": sample["bytes"] / dt / 1e9, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample["desc"], "seconds": dt}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32 transform, e4m3 codes", "data": "synthetic",
+                "config": {"workload": "llama600m-selective: 13 fc2 1536x6144 rank-32 GIFT + 60 Euclidean "
+                                       "(30x 1536x1536, 30x 1536x6144), E4M3 per-tensor, R=8",
+                           "gift_layers": len(gl), "euclid_tensors": len(eu), "replicas": R,
+                           "gradient_bytes_per_step": grad_bytes, "l2": "inputs exceed L2 (no flush)",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": kernels_per_step * args.steps, "stages": stages,
+                "factor_refresh": {"ms_per_layer": factor_ms, "syrk_tflops": syrk_flops / (factor_ms * 1e-3) / 1e12,
+                                   "note": "whole refresh (SYRK + rank-32 subspace iteration + Jacobi) per layer; "
+                                           "TFLOP/s counts the a^T a flops only"},
+                "device_status": status_word}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes):
+    """Same step through the public API with host buffers: per step, copy every replica
+    gradient from pinned host memory, run the codec, read the decoded / averaged results
+    back to pinned host memory."""
+    import torch
+    host_in, dev_in = [], []
+    for L in gl + eu:
+        for W in L["W"]:
+            h = torch.empty(W.shape, dtype=torch.float32, pin_memory=True)
+            h.copy_(W)
+            host_in.append(h)
+            dev_in.append(W)
+    outs = [L["out"] for L in gl] + [E["avg"] for E in eu]
+    host_out = [torch.empty(o.shape, dtype=torch.float32, pin_memory=True) for o in outs]
+    h2d = sum(h.numel() * 4 for h in host_in)
+    d2h = sum(h.numel() * 4 for h in host_out)
+    torch.cuda.synchronize()
+    steps = max(1, args.e2e_steps)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        for _, g in graphs:
+            g.replay()
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": grad_bytes / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    main_gift(args)
+
+
+if __name__ == "__main__":
+    main()

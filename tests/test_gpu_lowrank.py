@@ -28,16 +28,24 @@ def make_layer(d_out, d_in, T, exponent, seed, rank=32, R=1, dtype=torch.float32
     return [W.cpu().numpy() for W in Ws], F32, a
 
 
+def _ordinal(codes, fmt):
+    """Position of each code on the number line (sign-magnitude codes -> signed integers)."""
+    c = codes.astype(np.int64)
+    nb = 4 if fmt == "nvfp4" else 8
+    mag = c & ((1 << (nb - 1)) - 1)
+    return np.where(c >> (nb - 1), -mag, mag)
+
+
 def oracle_codes_close(got, want, fmt):
-    """Codes of two nearly equal tensors: equal, or one code step apart on few elements."""
+    """Codes of two nearly equal tensors: equal, or adjacent codes on a small fraction."""
+    if fmt == "nvfp4":
+        got = np.stack([got & 0xF, got >> 4], -1)
+        want = np.stack([want & 0xF, want >> 4], -1)
     diff = got != want
     frac = np.count_nonzero(diff) / diff.size
     assert frac < 2e-3, frac
-    if fmt in ("e4m3", "e5m2"):
-        f = O.FORMATS[fmt]
-        vg, vw = O.decode(got[diff], f), O.decode(want[diff], f)
-        step = np.abs(vw) * 2.0 ** -f.mbits + f.min_subnormal
-        assert np.all(np.abs(vg - vw) <= step * 1.0001)
+    dist = np.abs(_ordinal(got[diff], fmt) - _ordinal(want[diff], fmt))
+    assert np.all(dist <= 1), np.max(dist)
 
 
 @pytest.fixture(scope="module")
@@ -96,11 +104,15 @@ def test_lowrank_decode_and_roundtrip(which, request):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert rel_fro(Wo.cpu().numpy(), O.lowrank_unwhiten(X, F)) <= TOL
-    # lossless format: map back inverts the whitening (common confusions: lossless GIFT == baseline)
+    # lossless format: map back inverts the whitening (common confusions: lossless GIFT == baseline).
+    # Each direction is within 1e-5 of the oracle; the composition is not: whitening cancels
+    # sigma^-1/2 W against the rank-r term, so one FP32 rounding (u = 2^-24) of that term
+    # comes back multiplied by sqrt(mu_1 / sigma) in the map back.  Bound: 1e-5 + 8 u sqrt(mu_1/sigma).
     enc = encode(f, W, "f32")
     G.gift_decode(ctx(), f, enc["_dev"][0], False, "f32", "tensor", d_out, d_in, Wo, ws=w)
     torch.cuda.synchronize()
-    assert rel_fro(Wo.cpu().numpy(), W) <= TOL
+    tol_rt = TOL + 8 * 2.0 ** -24 * np.sqrt(float(F.mu[0]) / float(F.sigma))
+    assert rel_fro(Wo.cpu().numpy(), W) <= tol_rt
     # decode straight from codes = dequantise then map back
     e8 = encode(f, W, "e4m3")
     G.gift_decode(ctx(), f, e8["_dev"][0], True, "e4m3", "tensor", d_out, d_in, Wo, scales=e8["_dev"][1], ws=w)
