@@ -75,6 +75,7 @@ struct FactorWs {
   int k = 0, gsplits = 1, ysplits = 1;
   float *Y = nullptr, *Q = nullptr, *yparts = nullptr;
   double *Q64 = nullptr, *Gp = nullptr, *G = nullptr, *Rinv = nullptr, *V = nullptr, *ev = nullptr, *tr = nullptr;
+  double *sq = nullptr;     // per-CTA partial sums of a^2
   // CHOL
   double *A64 = nullptr, *Ai64 = nullptr, *work = nullptr;
   float *Gf = nullptr;
@@ -107,6 +108,7 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
     w.V = c.take<double>(64 * 64);
     w.ev = c.take<double>(64);
     w.tr = c.take<double>(1);
+    w.sq = c.take<double>((size_t)trace_partials(sms));
   } else if (kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED) {
     const int nmax = d_in > d_out ? d_in : d_out;
     w.A64 = c.take<double>((size_t)d_in * d_in);
@@ -330,7 +332,7 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
 
   if (f->kind == GIFT_XF_LOWRANK) {
     const int k = w.k;
-    CK(launch_trace(L, w.A, d_in, w.tr));
+    CK(launch_trace_from_activations(L, a, a_dt == GIFT_DT_BF16, T, d_in, w.sq, w.tr));
     auto cholqr = [&](const float *in, float *out) -> cudaError_t {
       DgemmArgs g{};
       g.A = in; g.B = in; g.C = w.Gp;

@@ -78,23 +78,55 @@ cudaError_t launch_philox_gaussian(const Launch &L, float *out, size_t n, uint64
 }
 
 // =====================================================================================
-// trace of an n x n FP32 matrix, FP64 accumulation in a fixed order (one CTA)
+// tr(A) = (1/T) sum_t sum_i a_ti^2 straight from the activations, in FP64: per-CTA partial
+// sums over a fixed grid-stride partition, then one thread adds the partials in order.
+// (The trace fixes sigma = (tr A - sum mu) / (d_in - r), a difference of nearly equal
+// numbers for steep spectra, so it is not taken from the FP32 diagonal of A.)
 // =====================================================================================
-__global__ void __launch_bounds__(256) k_trace(const float *__restrict__ A, int n, double *tr) {
+template <typename T>
+__device__ __forceinline__ double ld64(const T *p, size_t i);
+template <>
+__device__ __forceinline__ double ld64<float>(const float *p, size_t i) { return (double)p[i]; }
+template <>
+__device__ __forceinline__ double ld64<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+  return (double)__bfloat162float(p[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_sumsq_partial(const T *__restrict__ a, size_t n, double *__restrict__ part) {
   __shared__ double s[256];
   double acc = 0.0;
-  for (int i = threadIdx.x; i < n; i += 256) acc += (double)A[(size_t)i * n + i];
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const double v = ld64<T>(a, i);
+    acc = fma(v, v, acc);
+  }
   s[threadIdx.x] = acc;
   __syncthreads();
   for (int w = 128; w > 0; w >>= 1) {
     if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) tr[0] = s[0];
+  if (threadIdx.x == 0) part[blockIdx.x] = s[0];
 }
 
-cudaError_t launch_trace(const Launch &L, const float *A, int n, double *tr) {
-  k_trace<<<1, 256, 0, L.stream>>>(A, n, tr);
+__global__ void k_sum_partials(const double *__restrict__ part, int nb, double scale, double *out) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < nb; ++i) s += part[i];
+    out[0] = s * scale;
+  }
+}
+
+int trace_partials(int sms) { return sms * 4; }
+
+cudaError_t launch_trace_from_activations(const Launch &L, const void *a, bool bf16, int T, int d, double *part,
+                                          double *tr) {
+  const size_t n = (size_t)T * d;
+  const int nb = trace_partials(L.sms);
+  if (bf16) k_sumsq_partial<__nv_bfloat16><<<nb, 256, 0, L.stream>>>(reinterpret_cast<const __nv_bfloat16 *>(a), n, part);
+  else k_sumsq_partial<float><<<nb, 256, 0, L.stream>>>(reinterpret_cast<const float *>(a), n, part);
+  k_sum_partials<<<1, 32, 0, L.stream>>>(part, nb, 1.0 / (double)T, tr);
   return cudaGetLastError();
 }
 

@@ -104,7 +104,9 @@ size_t chol_inv_work_doubles(int n);
 
 // ---- factor.cu --------------------------------------------------------------------------
 cudaError_t launch_philox_gaussian(const Launch &L, float *out, size_t n, uint64_t seed);
-cudaError_t launch_trace(const Launch &L, const float *A, int n, double *tr);
+int trace_partials(int sms);
+cudaError_t launch_trace_from_activations(const Launch &L, const void *a, bool bf16, int T, int d, double *part,
+                                          double *tr);
 cudaError_t launch_small_chol_rinv(const Launch &L, const double *G, int k, double *Rinv);
 cudaError_t launch_jacobi(const Launch &L, const double *B, int k, double *evals, double *V);
 cudaError_t launch_lowrank_outputs(const Launch &L, const float *Q, int d_in, int k, const double *V,
