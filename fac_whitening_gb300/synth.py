@@ -43,20 +43,40 @@ def gaussian(shape, seed: int, device="cpu", dtype=torch.float32) -> torch.Tenso
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dtype)
 
 
-def haar_orthogonal(n: int, seed: int, device="cpu", dtype=torch.float32) -> torch.Tensor:
-    """A Haar-distributed random orthogonal n x n matrix.
+_BASE_ROTATIONS = {}
 
-    QR of a Gaussian matrix with the signs of R's diagonal folded into Q
-    (F. Mezzadri, "How to generate random matrices from the classical compact
-    groups", Notices of the AMS, 2007).
+
+def _base_rotation(n: int) -> torch.Tensor:
+    """One Haar-distributed n x n orthogonal matrix per size (host QR, cached per process).
+
+    QR of a Gaussian matrix with the signs of R's diagonal folded into Q (F. Mezzadri,
+    "How to generate random matrices from the classical compact groups", Notices of
+    the AMS, 2007).  Computed on the host so that no device linear-algebra library is
+    needed; FP64 up to n = 2048, FP32 above.
     """
-    g = _gen(seed, device)
-    work = torch.float64 if torch.device(device).type == "cpu" else torch.float32
-    z = torch.randn(n, n, generator=g, device=device, dtype=work)
-    q, r = torch.linalg.qr(z)
-    d = torch.sign(torch.diagonal(r))
-    d[d == 0] = 1
-    return (q * d.unsqueeze(0)).to(dtype)
+    if n not in _BASE_ROTATIONS:
+        g = _gen(SEED_BASE + n, "cpu")
+        work = torch.float64 if n <= 2048 else torch.float32
+        z = torch.randn(n, n, generator=g, dtype=work)
+        q, r = torch.linalg.qr(z)
+        d = torch.sign(torch.diagonal(r))
+        d[d == 0] = 1
+        _BASE_ROTATIONS[n] = (q * d.unsqueeze(0)).contiguous()
+    return _BASE_ROTATIONS[n]
+
+
+def haar_orthogonal(n: int, seed: int, device="cpu", dtype=torch.float32) -> torch.Tensor:
+    """A random orthogonal n x n matrix for `seed`: Q_base P D.
+
+    Q_base is the per-size Haar matrix of _base_rotation; P is a seeded random column
+    permutation and D seeded random signs, so every seed gives a different dense
+    rotation (Q_base P D is orthogonal and, Q_base being Haar, Haar-distributed).
+    """
+    g = _gen(seed, "cpu")
+    perm = torch.randperm(n, generator=g)
+    signs = torch.randint(0, 2, (n,), generator=g).to(torch.float64) * 2 - 1
+    q = _base_rotation(n)[:, perm] * signs.to(_base_rotation(n).dtype).unsqueeze(0)
+    return q.to(device=device, dtype=dtype)
 
 
 def spectrum_power_law(d: int, exponent: float, device="cpu") -> torch.Tensor:
