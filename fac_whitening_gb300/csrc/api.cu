@@ -8,12 +8,6 @@
 
 #include "kernels.cuh"
 
-struct gift_ctx {
-  int device;
-  int sms;
-  int subspace_iters;
-};
-
 using namespace gift;
 
 namespace {

@@ -3,6 +3,13 @@
 
 #include "common.cuh"
 
+// Host context behind the opaque gift_ctx handle.
+struct gift_ctx {
+  int device;
+  int sms;
+  int subspace_iters;
+};
+
 namespace gift {
 
 struct Launch {

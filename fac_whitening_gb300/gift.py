@@ -67,6 +67,8 @@ def _declare(lib):
         "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
                              _vp, _vp]),
         "gift_boundary_hit_rate": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
+        "gift_encode_lowrank_noalloc": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _vp, _vp, _vp, _vp,
+                                             _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -259,3 +261,12 @@ def gift_boundary_hit_rate(ctx: Context, W, fmt: str, scaling: str, counts, ws=N
     _check(lib().gift_boundary_hit_rate(ctx.handle, _p(W), d_out, d_in, FMT[fmt], SCALING[scaling], _p(counts),
                                         _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
                                         _stream(stream)), "gift_boundary_hit_rate")
+
+
+def gift_encode_lowrank_noalloc(ctx: Context, f: Factor, W, fmt: str, codes, scales, amax_in=None, amax_out=None,
+                                status=None, stream=None):
+    """Rank-r encode without a workspace (scratch lives inside the library; see gift.h)."""
+    d_out, d_in = W.shape
+    _check(lib().gift_encode_lowrank_noalloc(ctx.handle, _fptr(f), _p(W), d_out, d_in, FMT[fmt], _p(amax_in),
+                                             _p(codes), _p(scales), _p(amax_out), _p(status), _stream(stream)),
+           "gift_encode_lowrank_noalloc")

@@ -250,6 +250,25 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
                                    unsigned long long *d_counts, void *ws, size_t ws_bytes,
                                    int *d_status, cudaStream_t stream);
 
+/* Rank-r encode that allocates nothing (the paper has no counterpart; this is a library
+ * convenience).  Same result as gift_encode with a LOWRANK factor, E4M3 or E5M2 and
+ * per-tensor scaling, but without a caller workspace: for callers that cannot allocate
+ * device memory at the point where they encode, such as code running inside a gradient or
+ * communication hook while the framework's allocator must not grow, or C programs with no
+ * allocator of their own.  Its scratch (about 8.5 MiB) is a fixed array inside the library,
+ * present on every GPU that loads it until the process exits.
+ *  Limits: d_out <= 4096, and the split-K projection partials must fit the scratch
+ *  (ceil-split count x d_out x 32 floats <= 2^21); beyond them the call returns
+ *  GIFT_ERR_INVALID_ARG and enqueues nothing.
+ *  Set-up: the first call on a device (with that device current) looks up the array's
+ *  device address; make that first call before any stream capture begins.
+ *  Concurrency: all calls on a device share the scratch; calls whose GPU work overlaps
+ *  (unordered streams) race on it.  Order them on one stream or with events.
+ *  amax_in, amax_out, d_status may be NULL; scales receives one FP32 value. */
+gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
+                                        gift_format fmt, const float *amax_in, void *codes, float *scales,
+                                        float *amax_out, int *d_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
