@@ -276,8 +276,10 @@ def main_gift(args):
                 G.gift_amax(ctx, None, E["W"][r], FMT, "tensor", E["shared"], ws=ws, status=st)
 
     def e_encode():
+        # replicas in reverse order of their amax pass: the most recently read ones are
+        # still in L2 when their pack pass runs
         for E in eu:
-            for r in range(R):
+            for r in reversed(range(R)):
                 G.gift_encode(ctx, None, E["W"][r], FMT, "tensor", E["codes"][r], E["scales"][r],
                               amax_in=E["shared"], ws=ws, status=st)
 

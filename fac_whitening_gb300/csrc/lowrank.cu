@@ -23,12 +23,27 @@ namespace gift {
 constexpr int kProjRows = 128;
 constexpr int kProjChunk = 32;
 
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+  const unsigned saddr = (unsigned)__cvta_generic_to_shared(smem);
+  const int src = valid ? 16 : 0;   // 0 bytes read: the 16-byte destination is zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(src));
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool valid) {
+  const unsigned saddr = (unsigned)__cvta_generic_to_shared(smem);
+  const int src = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(saddr), "l"(gmem), "r"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
 template <bool VEC>
 __global__ void __launch_bounds__(256, 2) k_lr_proj(const float *__restrict__ X, int d_out, int d_in,
                                                     const float *__restrict__ U, int rank,
                                                     float *__restrict__ part, int jspan) {
-  __shared__ __align__(16) float Xs[kProjRows][36];
-  __shared__ __align__(16) float Us[kProjChunk][32];
+  // two stages of (X chunk, U chunk); stage buffers are reused for the final combine
+  __shared__ __align__(16) float Xs[2][kProjRows][36];
+  __shared__ __align__(16) float Us[2][kProjChunk][32];
   const int tid = threadIdx.x;
   const int tz = tid >> 7, t = tid & 127, tx = t & 7, ty = t >> 3;
   const int r0 = blockIdx.x * kProjRows;
@@ -40,30 +55,49 @@ __global__ void __launch_bounds__(256, 2) k_lr_proj(const float *__restrict__ X,
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[i][k] = 0.0f;
 
-  for (int j0 = jbeg; j0 < jend; j0 += kProjChunk) {
+  // Stage chunk j0 into buffer b.  The vector path uses cp.async (16-byte X pieces,
+  // 4-byte U elements, zero-filled outside the matrix); the scalar path plain loads.
+  auto stage = [&](int b, int j0) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int idx = q * 256 + tid;
       const int row = idx >> 3, c4 = idx & 7;
       const int gr = r0 + row, gc = j0 + 4 * c4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (VEC) {
-        if (gr < d_out && gc < jend) v = *reinterpret_cast<const float4 *>(X + (size_t)gr * d_in + gc);
-      } else if (gr < d_out) {
-        const float *p = X + (size_t)gr * d_in;
-        if (gc < jend) v.x = p[gc];
-        if (gc + 1 < jend) v.y = p[gc + 1];
-        if (gc + 2 < jend) v.z = p[gc + 2];
-        if (gc + 3 < jend) v.w = p[gc + 3];
+        const bool ok = gr < d_out && gc < jend;
+        cp_async16(&Xs[b][row][4 * c4], ok ? (const void *)(X + (size_t)gr * d_in + gc) : (const void *)X, ok);
+      } else {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gr < d_out) {
+          const float *p = X + (size_t)gr * d_in;
+          if (gc < jend) v.x = p[gc];
+          if (gc + 1 < jend) v.y = p[gc + 1];
+          if (gc + 2 < jend) v.z = p[gc + 2];
+          if (gc + 3 < jend) v.w = p[gc + 3];
+        }
+        *reinterpret_cast<float4 *>(&Xs[b][row][4 * c4]) = v;
       }
-      *reinterpret_cast<float4 *>(&Xs[row][4 * c4]) = v;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int idx = q * 256 + tid;
       const int jj = idx >> 5, k = idx & 31;
       const int gj = j0 + jj;
-      Us[jj][k] = (gj < jend && k < rank) ? U[(size_t)gj * rank + k] : 0.0f;
+      const bool ok = gj < jend && k < rank;
+      if (VEC) cp_async4(&Us[b][jj][k], ok ? (const void *)(U + (size_t)gj * rank + k) : (const void *)U, ok);
+      else Us[b][jj][k] = ok ? U[(size_t)gj * rank + k] : 0.0f;
+    }
+  };
+
+  int b = 0;
+  if (jbeg < jend) stage(0, jbeg);
+  if (VEC) cp_async_commit();
+  for (int j0 = jbeg; j0 < jend; j0 += kProjChunk) {
+    const bool more = j0 + kProjChunk < jend;
+    if (more) stage(b ^ 1, j0 + kProjChunk);
+    if (VEC) {
+      cp_async_commit();
+      cp_async_wait<1>();   // the current stage has landed
     }
     __syncthreads();
 #pragma unroll
@@ -71,24 +105,27 @@ __global__ void __launch_bounds__(256, 2) k_lr_proj(const float *__restrict__ X,
       const int j = 16 * tz + jj;
       float4 a[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(&Xs[ty + 16 * i][j]);
+      for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(&Xs[b][ty + 16 * i][j]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 b = *reinterpret_cast<const float4 *>(&Us[j + q][4 * tx]);
+        const float4 bb = *reinterpret_cast<const float4 *>(&Us[b][j + q][4 * tx]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float x = (q == 0) ? a[i].x : (q == 1) ? a[i].y : (q == 2) ? a[i].z : a[i].w;
-          acc[i][0] = fmaf(x, b.x, acc[i][0]);
-          acc[i][1] = fmaf(x, b.y, acc[i][1]);
-          acc[i][2] = fmaf(x, b.z, acc[i][2]);
-          acc[i][3] = fmaf(x, b.w, acc[i][3]);
+          acc[i][0] = fmaf(x, bb.x, acc[i][0]);
+          acc[i][1] = fmaf(x, bb.y, acc[i][1]);
+          acc[i][2] = fmaf(x, bb.z, acc[i][2]);
+          acc[i][3] = fmaf(x, bb.w, acc[i][3]);
         }
       }
     }
     __syncthreads();
+    b ^= 1;
   }
+  if (VEC) cp_async_wait<0>();
+  __syncthreads();
   // combine the two chunk halves (tz) through shared memory, then write the slice partial
-  float *red = &Xs[0][0];
+  float *red = &Xs[0][0][0];
   if (tz == 1) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -102,35 +139,47 @@ __global__ void __launch_bounds__(256, 2) k_lr_proj(const float *__restrict__ X,
       const int row = r0 + ty + 16 * i;
       if (row >= d_out) continue;
       const float4 o = *reinterpret_cast<const float4 *>(red + (ty + 16 * i) * 32 + 4 * tx);
-      const float4 s = make_float4(__fadd_rn(acc[i][0], o.x), __fadd_rn(acc[i][1], o.y),
-                                   __fadd_rn(acc[i][2], o.z), __fadd_rn(acc[i][3], o.w));
-      *reinterpret_cast<float4 *>(part + ((size_t)blockIdx.y * d_out + row) * 32 + 4 * tx) = s;
+      const float4 sum = make_float4(__fadd_rn(acc[i][0], o.x), __fadd_rn(acc[i][1], o.y),
+                                     __fadd_rn(acc[i][2], o.z), __fadd_rn(acc[i][3], o.w));
+      *reinterpret_cast<float4 *>(part + ((size_t)blockIdx.y * d_out + row) * 32 + 4 * tx) = sum;
     }
   }
 }
 
 // -------------------------------------------------------------------------------------
-// finalize: Pc[row][k] = c_k * sum_s part[s][row][k] (FP64 sum in slice order)
+// finalize: Pc[row][k] = c_k * sum_s part[s][row][k]
 //   whitening  c_k = mu_k^-1/2 - sigma^-1/2;  map back  c_k = mu_k^1/2 - sigma^1/2; 0 for k >= rank
+// The 32 coefficients are formed once per CTA in FP64; the slice partials are added in
+// slice order with a compensated (Kahan) FP32 sum, and the product is taken in FP64.
 // -------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_lr_finalize(const float *__restrict__ part, int nsplit, int d_out,
                                                      const float *__restrict__ mu, const float *__restrict__ sigma,
                                                      int rank, bool inverse, float *__restrict__ Pc, int *status) {
+  __shared__ double coef[32];
+  if (threadIdx.x < 32) {
+    const int k = threadIdx.x;
+    double c = 0.0;
+    if (k < rank) {
+      const double m = (double)mu[k], sg = (double)sigma[0];
+      if (!(m > 0.0) || !(sg > 0.0)) {
+        if (blockIdx.x == 0) set_status(status, GIFT_ERR_NOT_PD);
+      } else {
+        c = inverse ? (sqrt(m) - sqrt(sg)) : (1.0 / sqrt(m) - 1.0 / sqrt(sg));
+      }
+    }
+    coef[k] = c;
+  }
+  __syncthreads();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= d_out * 32) return;
-  const int k = idx & 31;
-  double s = 0.0;
-  for (int sp = 0; sp < nsplit; ++sp) s += (double)part[(size_t)sp * d_out * 32 + idx];
-  double c = 0.0;
-  if (k < rank) {
-    const double m = (double)mu[k], sg = (double)sigma[0];
-    if (!(m > 0.0) || !(sg > 0.0)) {
-      set_status(status, GIFT_ERR_NOT_PD);
-    } else {
-      c = inverse ? (sqrt(m) - sqrt(sg)) : (1.0 / sqrt(m) - 1.0 / sqrt(sg));
-    }
+  float s = 0.0f, comp = 0.0f;
+  for (int sp = 0; sp < nsplit; ++sp) {
+    const float y = __fsub_rn(part[(size_t)sp * d_out * 32 + idx], comp);
+    const float t = __fadd_rn(s, y);
+    comp = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
   }
-  Pc[idx] = (float)(c * s);
+  Pc[idx] = (float)(coef[idx & 31] * ((double)s - (double)comp));
 }
 
 // -------------------------------------------------------------------------------------
@@ -392,7 +441,7 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
   const int per = (chunks + nsplit - 1) / nsplit;
   const int jspan = per * kProjChunk;
   dim3 grid((d_out + kProjRows - 1) / kProjRows, nsplit);
-  const bool vec = (d_in % 4 == 0) && aligned16(X);
+  const bool vec = (d_in % 4 == 0) && aligned16(X) && (((uintptr_t)U & 3u) == 0);
   if (vec) k_lr_proj<true><<<grid, 256, 0, L.stream>>>(X, d_out, d_in, U, rank, part, jspan);
   else k_lr_proj<false><<<grid, 256, 0, L.stream>>>(X, d_out, d_in, U, rank, part, jspan);
   return cudaGetLastError();
