@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=13, help="geometry-aware layers (13 in the workload)")
     p.add_argument("--euclid", type=int, default=30, help="Euclidean tensors of each shape (30 in the workload)")
+    p.add_argument("--streams", type=int, default=4, help="streams the independent tensors of a stage spread over")
     return p.parse_args()
 
 
@@ -239,7 +240,9 @@ def main_gift(args):
     # ---- buffers -----------------------------------------------------------------------
     ws_bytes = max(G.gift_workspace_bytes(ctx, op, k, FMT, "tensor", d_out, d_in)
                    for op in ("encode", "decode", "amax") for k in ("lowrank", "identity"))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    nstr = max(1, args.streams)
+    streams = [torch.cuda.Stream() for _ in range(nstr)]
+    wss = [torch.zeros(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(nstr)]
 
     def codes_for(spec):
         return ([torch.empty(spec.d_out * spec.d_in, dtype=torch.uint8, device=dev) for _ in range(R)],
@@ -255,38 +258,51 @@ def main_gift(args):
         E["avg"] = torch.empty(E["spec"].d_out, E["spec"].d_in, dtype=torch.float32, device=dev)
         E["shared"] = shared[j:j + 1]
 
+    def fork_join(items, fn):
+        """Run fn(item, ws) for independent items round-robin over the side streams; the
+        current stream waits for all of them (one join per stage group)."""
+        main = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(main)
+        for s in streams:
+            s.wait_stream(main)
+        for i, it in enumerate(items):
+            with torch.cuda.stream(streams[i % nstr]):
+                fn(it, wss[i % nstr])
+        for s in streams:
+            main.wait_stream(s)
+
     # ---- stage groups ------------------------------------------------------------------
     def g_encode():
-        for f, L in zip(factors, gl):
-            for r in range(R):
-                G.gift_encode(ctx, f, L["W"][r], FMT, "tensor", L["codes"][r], L["scales"][r], ws=ws, status=st)
+        fork_join([(f, L, r) for f, L in zip(factors, gl) for r in range(R)],
+                  lambda it, w: G.gift_encode(ctx, it[0], it[1]["W"][it[2]], FMT, "tensor", it[1]["codes"][it[2]],
+                                              it[1]["scales"][it[2]], ws=w, status=st))
 
     def g_reduce():
-        for L in gl:
-            G.gift_replica_reduce(ctx, L["codes"], L["scales"], FMT, "tensor", d_out, d_in, L["avg"], status=st)
+        fork_join(gl, lambda L, w: G.gift_replica_reduce(ctx, L["codes"], L["scales"], FMT, "tensor", d_out, d_in,
+                                                         L["avg"], status=st))
 
     def g_decode():
-        for f, L in zip(factors, gl):
-            G.gift_decode(ctx, f, L["avg"], False, "f32", "tensor", d_out, d_in, L["out"], ws=ws, status=st)
+        fork_join(list(zip(factors, gl)),
+                  lambda it, w: G.gift_decode(ctx, it[0], it[1]["avg"], False, "f32", "tensor", d_out, d_in,
+                                              it[1]["out"], ws=w, status=st))
 
     def e_amax():
         shared.zero_()
-        for E in eu:
-            for r in range(R):
-                G.gift_amax(ctx, None, E["W"][r], FMT, "tensor", E["shared"], ws=ws, status=st)
+        fork_join([(E, r) for E in eu for r in range(R)],
+                  lambda it, w: G.gift_amax(ctx, None, it[0]["W"][it[1]], FMT, "tensor", it[0]["shared"], ws=w,
+                                            status=st))
 
     def e_encode():
         # replicas in reverse order of their amax pass: the most recently read ones are
         # still in L2 when their pack pass runs
-        for E in eu:
-            for r in reversed(range(R)):
-                G.gift_encode(ctx, None, E["W"][r], FMT, "tensor", E["codes"][r], E["scales"][r],
-                              amax_in=E["shared"], ws=ws, status=st)
+        fork_join([(E, r) for E in eu for r in reversed(range(R))],
+                  lambda it, w: G.gift_encode(ctx, None, it[0]["W"][it[1]], FMT, "tensor", it[0]["codes"][it[1]],
+                                              it[0]["scales"][it[1]], amax_in=it[0]["shared"], ws=w, status=st))
 
     def e_reduce():
-        for E in eu:
-            s = E["spec"]
-            G.gift_replica_reduce(ctx, E["codes"], E["scales"], FMT, "tensor", s.d_out, s.d_in, E["avg"], status=st)
+        fork_join(eu, lambda E, w: G.gift_replica_reduce(ctx, E["codes"], E["scales"], FMT, "tensor",
+                                                         E["spec"].d_out, E["spec"].d_in, E["avg"], status=st))
 
     groups = [("gift_encode", g_encode), ("gift_reduce", g_reduce), ("gift_decode", g_decode),
               ("euclid_amax", e_amax), ("euclid_encode", e_encode), ("euclid_reduce", e_reduce)]
@@ -374,7 +390,7 @@ def main_gift(args):
     # ---- end to end through the public API with host buffers --------------------------
     e2e = None
     if not args.no_e2e and rank == 0:
-        e2e = run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes)
+        e2e = run_e2e(args, G, ctx, gl, eu, factors, R, wss[0], st, graphs, dev, grad_bytes)
 
     # ---- CPU baseline (oracle on a bounded sample) --------------------------------------
     cpu = None
@@ -395,7 +411,7 @@ def main_gift(args):
                                        "(30x 1536x1536, 30x 1536x6144), E4M3 per-tensor, R=8",
                            "gift_layers": len(gl), "euclid_tensors": len(eu), "replicas": R,
                            "gradient_bytes_per_step": grad_bytes, "l2": "inputs exceed L2 (no flush)",
-                           "parallelism": f"replicas x{world}"},
+                           "parallelism": f"replicas x{world}", "streams_per_stage": nstr},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": kernels_per_step * args.steps, "stages": stages,
                 "factor_refresh": {"ms_per_layer": factor_ms, "syrk_tflops": syrk_flops / (factor_ms * 1e-3) / 1e12,

@@ -12,6 +12,8 @@ using namespace gift;
 
 namespace {
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 constexpr size_t kAlign = 256;
 
 // Bump allocator over the caller's workspace; with base == nullptr it only measures.
@@ -118,9 +120,13 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
   return w;
 }
 
-#define CK(expr)                                   \
-  do {                                             \
-    if ((expr) != cudaSuccess) return GIFT_ERR_CUDA; \
+#define CK(expr)                      \
+  do {                                \
+    const cudaError_t ck_e_ = (expr); \
+    if (ck_e_ != cudaSuccess) {       \
+      record_cuda_error(ck_e_);       \
+      return GIFT_ERR_CUDA;           \
+    }                                 \
   } while (0)
 
 Launch mk(const gift_ctx *ctx, int *st, cudaStream_t s) {
@@ -186,8 +192,10 @@ cudaError_t chol_unwhiten(const Launch &L, const gift_factor *f, const float *X,
   return launch_sgemm(L, g);
 }
 
-LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w, bool inverse) {
+LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w, bool inverse,
+                gift_precision prec) {
   LrApply a{};
+  a.terms = (prec == GIFT_PREC_TC) ? 1 : 3;
   a.X = X;
   a.U = f->U;
   a.Pc = w.Pc;
@@ -208,8 +216,16 @@ cudaError_t lr_prepare(const Launch &L, const gift_factor *f, const float *X, in
 
 }  // namespace
 
+namespace gift {
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = e; }
+}  // namespace gift
+
 // =========================================================================================
 extern "C" {
+
+const char *gift_last_error(void) {
+  return t_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda_error);
+}
 
 gift_status gift_create(gift_ctx **ctx, int device) {
   if (!ctx) return GIFT_ERR_INVALID_ARG;
@@ -405,7 +421,6 @@ static gift_status codec_common_checks(gift_ctx *ctx, const gift_factor *f, cons
 gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in, gift_format fmt,
                       gift_scaling scaling, gift_precision prec, const float *residual, float *amax_accum, void *ws,
                       size_t ws_bytes, int *d_status, cudaStream_t stream) {
-  (void)prec;
   gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
   if (cs != GIFT_OK) return cs;
   if (!amax_accum || fmt == GIFT_FMT_F32) return GIFT_ERR_INVALID_ARG;
@@ -418,7 +433,7 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   const size_t n = (size_t)d_out * d_in;
   if (kind == GIFT_XF_LOWRANK) {
     CK(lr_prepare(L, f, W, d_out, d_in, w, false));
-    LrApply a = lr_args(f, W, d_out, d_in, w, false);
+    LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = const_cast<float *>(residual);   // read only by the amax epilogue
     a.amax_ws = amax_accum;
     CK(launch_lr_apply(L, block ? LR_BLOCK_AMAX : LR_AMAX, fmt, a));
@@ -439,7 +454,6 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
                         gift_scaling scaling, gift_precision prec, const float *amax_in, float *residual,
                         void *codes, void *scales, float *tensor_scale, float *transformed_out, float *amax_out,
                         void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
-  (void)prec;
   gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
   if (cs != GIFT_OK) return cs;
   if (!codes) return GIFT_ERR_INVALID_ARG;
@@ -457,7 +471,7 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
 
   if (kind == GIFT_XF_LOWRANK) {
     CK(lr_prepare(L, f, W, d_out, d_in, w, false));
-    LrApply a = lr_args(f, W, d_out, d_in, w, false);
+    LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = residual;
     if (fmt == GIFT_FMT_F32) {
       a.out = static_cast<float *>(codes);
@@ -547,7 +561,6 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
                         const float *tensor_scale, gift_format fmt, gift_scaling scaling, gift_precision prec,
                         int d_out, int d_in, float *W_out, void *ws, size_t ws_bytes, int *d_status,
                         cudaStream_t stream) {
-  (void)prec;
   if (!ctx || !in || !W_out || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
   if ((const void *)W_out == in) return GIFT_ERR_INVALID_ARG;
   const bool codes_in = in_is_codes && fmt != GIFT_FMT_F32;
@@ -581,7 +594,7 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
     CK(launch_pack_f32(L, X, nullptr, n, W_out, nullptr));
   } else if (kind == GIFT_XF_LOWRANK) {
     CK(lr_prepare(L, f, X, d_out, d_in, w, true));
-    LrApply a = lr_args(f, X, d_out, d_in, w, true);
+    LrApply a = lr_args(f, X, d_out, d_in, w, true, prec);
     a.out = W_out;
     CK(launch_lr_apply(L, LR_STORE, GIFT_FMT_F32, a));
   } else {

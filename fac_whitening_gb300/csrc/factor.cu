@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(256) k_small_chol_rinv(const double *__restric
 
 cudaError_t launch_small_chol_rinv(const Launch &L, const double *G, int k, double *Rinv) {
   const int smem = 2 * 64 * 65 * (int)sizeof(double);
-  cudaError_t e = cudaFuncSetAttribute(k_small_chol_rinv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_dynamic_smem<k_small_chol_rinv>(smem);
   if (e != cudaSuccess) return e;
   k_small_chol_rinv<<<1, 256, smem, L.stream>>>(G, k, Rinv);
   return cudaGetLastError();
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kJacThreads) k_jacobi(const double *__restrict
 
 cudaError_t launch_jacobi(const Launch &L, const double *B, int k, double *evals, double *V) {
   const size_t smem = 2 * sizeof(double) * kJacMax * (kJacMax + 1);
-  cudaError_t e = cudaFuncSetAttribute(k_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem<k_jacobi>((int)smem);
   if (e != cudaSuccess) return e;
   k_jacobi<<<1, kJacThreads, smem, L.stream>>>(B, k, evals, V, L.status);
   return cudaGetLastError();

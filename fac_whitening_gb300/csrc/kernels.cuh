@@ -66,8 +66,30 @@ struct LrApply {
   float *tscale;
   float *amax_out;
   float *out;               // LR_STORE
+  int terms;                // tensor-core path: 1 = one TF32 product (TC), otherwise 3-term split (FP32)
 };
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
+// lowrank_tc.cu: the same apply on tcgen05 tensor cores (vectorised shapes only)
+bool lr_apply_tc_ok(const LrApply &a, int epi);
+cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply &a, bool single_term);
+
+// Sets a kernel's opt-in dynamic shared-memory size once per device and kernel (so no
+// attribute call happens inside a stream capture after the first eager call).  Keyed on the
+// kernel itself: instantiations that share a function type keep separate flags.
+template <auto Kernel>
+cudaError_t ensure_dynamic_smem(int bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  return e;
+}
+
+// Last CUDA error seen by a libgift call on this thread (see gift_last_error).
+void record_cuda_error(cudaError_t e);
 
 // ---- linalg.cu --------------------------------------------------------------------------
 // C[M x N] = alpha * op(A) op(B), FP32 accumulate.  op(A) = A (M x K, lda) or A^T (A is K x M).

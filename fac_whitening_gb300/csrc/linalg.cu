@@ -468,7 +468,7 @@ static cudaError_t chol_inv_rec(const Launch &L, double *A, double *Li, int ld, 
   double *Lb = Li + (size_t)o * ld + o;
   if (n <= kCholBase) {
     const int smem = 2 * kCholBase * (kCholBase + 1) * (int)sizeof(double);
-    cudaError_t e0 = cudaFuncSetAttribute(k_chol_inv_small, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e0 = ensure_dynamic_smem<k_chol_inv_small>(smem);
     if (e0 != cudaSuccess) return e0;
     k_chol_inv_small<<<1, 256, smem, L.stream>>>(Ab, ld, Lb, ld, n, L.status);
     return cudaGetLastError();

@@ -470,6 +470,7 @@ static void apply_dispatch(const Launch &L, const LrApply &a, bool vec) {
 }
 
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a) {
+  if (lr_apply_tc_ok(a, epi)) return launch_lr_apply_tc(L, epi, fmt, a, a.terms == 1);
   bool vec = (a.d_in % 4 == 0) && aligned16(a.X) && (!a.R || aligned16(a.R)) && (!a.tout || aligned16(a.tout));
   if (epi == LR_STORE) vec = vec && aligned16(a.out);
   if (epi == LR_PACK_TENSOR || epi == LR_BLOCK) vec = vec && (((uintptr_t)a.codes & 3u) == 0);

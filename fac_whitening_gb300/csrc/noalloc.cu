@@ -70,7 +70,11 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   if (cudaGetDevice(&cur) != cudaSuccess || cur != ctx->device || cur < 0 || cur >= kMaxDevices)
     return GIFT_ERR_INVALID_ARG;
   float *base = nullptr;
-  if (scratch_address(cur, &base) != cudaSuccess) return GIFT_ERR_CUDA;
+  const cudaError_t se = scratch_address(cur, &base);
+  if (se != cudaSuccess) {
+    record_cuda_error(se);
+    return GIFT_ERR_CUDA;
+  }
   float *amax_ws = base;
   float *Pc = base + kNoAllocAmaxFloats;
   float *part = Pc + kNoAllocPcFloats;
@@ -91,6 +95,7 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.d_out = d_out;
   a.d_in = d_in;
   a.inverse = false;
+  a.terms = 3;
   a.codes = static_cast<uint8_t *>(codes);
   a.scales = scales;
   a.amax_out = amax_out;

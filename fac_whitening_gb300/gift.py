@@ -41,7 +41,10 @@ class GiftFactor(ctypes.Structure):
 
 class GiftError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == ERR_CUDA:
+            msg += f": {lib().gift_last_error().decode()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -55,6 +58,7 @@ def _declare(lib):
         "gift_set_option": (_i, [_vp, _i, ctypes.c_longlong]),
         "gift_status_string": (ctypes.c_char_p, [_i]),
         "gift_version": (_i, []),
+        "gift_last_error": (ctypes.c_char_p, []),
         "gift_workspace_bytes": (_sz, [_vp, _i, _i, _i, _i, _i, _i, _i, _i]),
         "gift_code_sizes": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
         "gift_factor_update": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _vp, _i, ctypes.c_uint64, _i,

@@ -144,6 +144,9 @@ void gift_destroy(gift_ctx *ctx);
 gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value);
 const char *gift_status_string(gift_status s);
 int gift_version(void); /* major * 1000 + minor */
+/* Text of the last CUDA runtime error that made a libgift call on this thread return
+ * GIFT_ERR_CUDA ("no CUDA error" if none); valid until the next failing call. */
+const char *gift_last_error(void);
 
 /* Bytes of caller-provided device workspace an operation needs (0 if none).
  * Host-only; returns (size_t)-1 for invalid arguments.  T is used by

@@ -48,7 +48,7 @@ def factor_to_gpu(kind, d_out, d_in, F=None, LA=None, LAinv=None, LG=None, LGinv
     return f
 
 
-def encode(f, W, fmt, scaling="tensor", amax_in=None, residual=None, Wt=None):
+def encode(f, W, fmt, scaling="tensor", amax_in=None, residual=None, Wt=None, prec="fp32"):
     """Run gift_encode; returns a dict of numpy outputs (codes shaped like the oracle's)."""
     Wt = t(W) if Wt is None else Wt
     d_out, d_in = Wt.shape
@@ -61,7 +61,7 @@ def encode(f, W, fmt, scaling="tensor", amax_in=None, residual=None, Wt=None):
     st = status()
     G.gift_encode(ctx(), f, Wt, fmt, scaling, codes, scales, tscale,
                   amax_in=None if amax_in is None else t(np.atleast_1d(amax_in)),
-                  residual=R, transformed_out=tout, amax_out=amax_out,
+                  residual=R, transformed_out=tout, amax_out=amax_out, prec=prec,
                   ws=ws("encode", kind, fmt, scaling, d_out, d_in), status=st)
     torch.cuda.synchronize()
     out = {"status": int(st.item()), "tout": tout.cpu().numpy(), "amax": amax_out.cpu().numpy()}

@@ -85,6 +85,20 @@ def test_lowrank_encode(which, fmt, scaling, request):
     oracle_codes_close(out, want, fmt, scaling)                # against the oracle's own transform
 
 
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("nvfp4", "tensor"), ("e5m2", "block128")])
+def test_lowrank_encode_tc_precision(c3, fmt, scaling):
+    # reduced-precision tensor-core path: transform within 2e-2, quantiser contract bit-exact
+    Ws, F, _ = c3
+    W = Ws[0]
+    f = factor_to_gpu("lowrank", *W.shape, F=F)
+    out = encode(f, W, fmt, scaling, prec="tc")
+    want = O.lowrank_whiten(W, F)
+    err = rel_fro(out["tout"], want)
+    assert err <= 2e-2, err
+    qg = O.quantize(out["tout"], fmt, scaling)
+    np.testing.assert_array_equal(out["codes"], qg["codes"])
+
+
 def test_lowrank_error_feedback(tiny):
     Ws, F, _ = tiny
     W = Ws[1]
