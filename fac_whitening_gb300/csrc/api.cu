@@ -41,6 +41,7 @@ struct CodecWs {
   float *Pc = nullptr;     // LOWRANK: d_out x 32
   float *xbuf = nullptr;   // transformed tensor (CHOL encode) or dequantised input (decode)
   float *tbuf = nullptr;   // CHOL_TWO_SIDED intermediate
+  float *split = nullptr;  // LOWRANK: TF32 term planes for the tensor-core apply
   int nsplit = 0;
   size_t bytes = 0;
 };
@@ -54,6 +55,7 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
     w.nsplit = lr_proj_splits(sms, d_out, d_in);
     w.part = c.take<float>((size_t)w.nsplit * d_out * 32);
     w.Pc = c.take<float>((size_t)d_out * 32);
+    w.split = c.take<float>(lr_pipe_split_floats(d_out, d_in));
   }
   if (kind != GIFT_XF_IDENTITY) {
     if (op == GIFT_OP_DECODE || kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED)
@@ -204,14 +206,28 @@ LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const
   a.d_out = d_out;
   a.d_in = d_in;
   a.inverse = inverse;
+  a.split = (d_in % 32 == 0) ? w.split : nullptr;
   return a;
 }
 
+// Projection and coefficients; for shapes the tensor-core apply takes, also the TF32 term
+// planes of Pc (by the finalize) and of U.
 cudaError_t lr_prepare(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w,
-                       bool inverse) {
+                       bool inverse, gift_precision prec) {
   cudaError_t e = launch_lr_proj(L, X, d_out, d_in, f->U, f->rank, w.part, w.nsplit);
   if (e != cudaSuccess) return e;
-  return launch_lr_finalize(L, w.part, w.nsplit, d_out, f->mu, f->sigma, f->rank, inverse, w.Pc);
+  const int terms = (prec == GIFT_PREC_TC) ? 1 : 3;
+  float *pc_terms = (d_in % 32 == 0) ? w.split : nullptr;
+  e = launch_lr_finalize(L, w.part, w.nsplit, d_out, f->mu, f->sigma, f->rank, inverse, w.Pc, pc_terms, terms);
+  if (e != cudaSuccess || !pc_terms) return e;
+  LrApply a{};
+  a.U = f->U;
+  a.rank = f->rank;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.terms = terms;
+  a.split = w.split;
+  return launch_lr_split_u(L, a);
 }
 
 }  // namespace
@@ -432,7 +448,7 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
   const size_t n = (size_t)d_out * d_in;
   if (kind == GIFT_XF_LOWRANK) {
-    CK(lr_prepare(L, f, W, d_out, d_in, w, false));
+    CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = const_cast<float *>(residual);   // read only by the amax epilogue
     a.amax_ws = amax_accum;
@@ -470,7 +486,7 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
   const bool block = (scaling == GIFT_SCALE_BLOCK128);
 
   if (kind == GIFT_XF_LOWRANK) {
-    CK(lr_prepare(L, f, W, d_out, d_in, w, false));
+    CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = residual;
     if (fmt == GIFT_FMT_F32) {
@@ -593,7 +609,7 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
   if (kind == GIFT_XF_IDENTITY) {
     CK(launch_pack_f32(L, X, nullptr, n, W_out, nullptr));
   } else if (kind == GIFT_XF_LOWRANK) {
-    CK(lr_prepare(L, f, X, d_out, d_in, w, true));
+    CK(lr_prepare(L, f, X, d_out, d_in, w, true, prec));
     LrApply a = lr_args(f, X, d_out, d_in, w, true, prec);
     a.out = W_out;
     CK(launch_lr_apply(L, LR_STORE, GIFT_FMT_F32, a));

@@ -47,7 +47,8 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
                            float *part, int nsplit);
 // Pc[row][k] = c_k * sum_s part[s][row][k]; c from (mu, sigma), inverse = map-back coefficients.
 cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
-                               const float *sigma, int rank, bool inverse, float *Pc);
+                               const float *sigma, int rank, bool inverse, float *Pc, float *pc_terms = nullptr,
+                               int terms = 3);
 // Fused apply V = alpha X + Pc U^T (+ R), alpha = sigma^-1/2 (or sigma^1/2 for the map back).
 enum LrEpi { LR_AMAX = 0, LR_PACK_TENSOR = 1, LR_BLOCK = 2, LR_NVFP4 = 3, LR_STORE = 4, LR_BLOCK_AMAX = 5 };
 struct LrApply {
@@ -67,10 +68,13 @@ struct LrApply {
   float *amax_out;
   float *out;               // LR_STORE
   int terms;                // tensor-core path: 1 = one TF32 product (TC), otherwise 3-term split (FP32)
+  float *split;             // TF32 term planes: Pc terms (3 x d_out x 32) then U terms (3 x d_in x 32)
 };
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
 // lowrank_tc.cu: the same apply on tcgen05 tensor cores (vectorised shapes only)
 bool lr_apply_tc_ok(const LrApply &a, int epi);
+size_t lr_pipe_split_floats(int d_out, int d_in);
+cudaError_t launch_lr_split_u(const Launch &L, const LrApply &a);
 cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply &a, bool single_term);
 
 // Sets a kernel's opt-in dynamic shared-memory size once per device and kernel (so no

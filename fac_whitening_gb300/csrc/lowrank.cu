@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(256, 2) k_lr_proj(const float *__restrict__ X,
 // -------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_lr_finalize(const float *__restrict__ part, int nsplit, int d_out,
                                                      const float *__restrict__ mu, const float *__restrict__ sigma,
-                                                     int rank, bool inverse, float *__restrict__ Pc, int *status) {
+                                                     int rank, bool inverse, float *__restrict__ Pc,
+                                                     float *__restrict__ pc_terms, int terms, int *status) {
   __shared__ double coef[32];
   if (threadIdx.x < 32) {
     const int k = threadIdx.x;
@@ -179,7 +180,20 @@ __global__ void __launch_bounds__(256) k_lr_finalize(const float *__restrict__ p
     comp = __fsub_rn(__fsub_rn(t, s), y);
     s = t;
   }
-  Pc[idx] = (float)(coef[idx & 31] * ((double)s - (double)comp));
+  const float pc = (float)(coef[idx & 31] * ((double)s - (double)comp));
+  Pc[idx] = pc;
+  if (pc_terms) {
+    // exact TF32 terms pc = t1 + t2 + t3 (each with its low 13 mantissa bits zero) for the
+    // tensor-core apply; plane q at pc_terms + q * d_out * 32
+    const float t1 = __uint_as_float((__float_as_uint(pc) + 0x1000u) & 0xFFFFE000u);
+    const float r1 = pc - t1;
+    const float t2 = __uint_as_float((__float_as_uint(r1) + 0x1000u) & 0xFFFFE000u);
+    pc_terms[idx] = t1;
+    if (terms > 1) {
+      pc_terms[(size_t)d_out * 32 + idx] = t2;
+      pc_terms[(size_t)2 * d_out * 32 + idx] = r1 - t2;
+    }
+  }
 }
 
 // -------------------------------------------------------------------------------------
@@ -448,9 +462,10 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
 }
 
 cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
-                               const float *sigma, int rank, bool inverse, float *Pc) {
+                               const float *sigma, int rank, bool inverse, float *Pc, float *pc_terms, int terms) {
   const int n = d_out * 32;
-  k_lr_finalize<<<(n + 255) / 256, 256, 0, L.stream>>>(part, nsplit, d_out, mu, sigma, rank, inverse, Pc, L.status);
+  k_lr_finalize<<<(n + 255) / 256, 256, 0, L.stream>>>(part, nsplit, d_out, mu, sigma, rank, inverse, Pc, pc_terms,
+                                                       terms, L.status);
   return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@
 // that scratch in one fixed array in device memory that the library itself declares, so
 // the call allocates nothing at all.
 //
-// The array (about 8.5 MiB) exists on every GPU that loads the library, for as long as the
+// The array (about 16 MiB) exists on every GPU that loads the library, for as long as the
 // process lives.  All calls on a device share it: two calls whose work overlaps on the GPU
 // (different streams without ordering between them) race on it and give wrong results, so
 // order them on one stream or with events.  The amax word is cleared by every call; the
@@ -25,10 +25,12 @@
 namespace {
 
 constexpr int kNoAllocMaxRows = 4096;                        // d_out limit
+constexpr int kNoAllocMaxCols = 16384;                       // d_in limit
 constexpr size_t kNoAllocAmaxFloats = 64;                    // one word, padded to 256 B
 constexpr size_t kNoAllocPcFloats = (size_t)kNoAllocMaxRows * 32;
 constexpr size_t kNoAllocPartFloats = (size_t)2 << 20;       // 8 MiB of projection partials
-constexpr size_t kNoAllocFloats = kNoAllocAmaxFloats + kNoAllocPcFloats + kNoAllocPartFloats;
+constexpr size_t kNoAllocSplitFloats = (size_t)3 * 32 * (kNoAllocMaxRows + kNoAllocMaxCols);   // 7.5 MiB
+constexpr size_t kNoAllocFloats = kNoAllocAmaxFloats + kNoAllocPcFloats + kNoAllocPartFloats + kNoAllocSplitFloats;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
@@ -63,7 +65,7 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   if (!f->U || !f->mu || !f->sigma || f->rank < 1 || f->rank > kMaxRank || f->rank > d_in)
     return GIFT_ERR_INVALID_ARG;
   // size limits of the fixed scratch
-  if (d_out > kNoAllocMaxRows) return GIFT_ERR_INVALID_ARG;
+  if (d_out > kNoAllocMaxRows || d_in > kNoAllocMaxCols) return GIFT_ERR_INVALID_ARG;
   const int nsplit = lr_proj_splits(ctx->sms, d_out, d_in);
   if ((size_t)nsplit * d_out * 32 > kNoAllocPartFloats) return GIFT_ERR_INVALID_ARG;
   int cur = -1;
@@ -78,13 +80,15 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   float *amax_ws = base;
   float *Pc = base + kNoAllocAmaxFloats;
   float *part = Pc + kNoAllocPcFloats;
+  float *split = part + kNoAllocPartFloats;
 
   Launch L;
   L.stream = stream;
   L.sms = ctx->sms;
   L.status = d_status;
   if (launch_lr_proj(L, W, d_out, d_in, f->U, f->rank, part, nsplit) != cudaSuccess) return GIFT_ERR_CUDA;
-  if (launch_lr_finalize(L, part, nsplit, d_out, f->mu, f->sigma, f->rank, false, Pc) != cudaSuccess)
+  float *pc_terms = (d_in % 32 == 0) ? split : nullptr;
+  if (launch_lr_finalize(L, part, nsplit, d_out, f->mu, f->sigma, f->rank, false, Pc, pc_terms, 3) != cudaSuccess)
     return GIFT_ERR_CUDA;
   LrApply a{};
   a.X = W;
@@ -96,6 +100,8 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.d_in = d_in;
   a.inverse = false;
   a.terms = 3;
+  a.split = pc_terms;
+  if (pc_terms && launch_lr_split_u(L, a) != cudaSuccess) return GIFT_ERR_CUDA;
   a.codes = static_cast<uint8_t *>(codes);
   a.scales = scales;
   a.amax_out = amax_out;
