@@ -60,6 +60,29 @@ def dist_info():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def dist_init(world, backend):
+    """One process per GPU (torch.distributed.run sets RANK / WORLD_SIZE / MASTER_*)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend)
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's time: the job is done when every rank is."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, bytes_per_rank, ms):
+    """Whole-job throughput in GB/s: every rank codes its own replicas (weak scaling)."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -202,9 +225,7 @@ def main_gift(args):
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    dist_init(world, "nccl")
     ctx = G.Context(local)
     hbm_peak, bf16_peak, peak_kind = peaks()
 
@@ -356,16 +377,12 @@ def main_gift(args):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms = total_ms / args.steps
     status_word = int(st.item())
     group_ms = {name: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
                 for i, (name, _) in enumerate(graphs)}
-    value = world * grad_bytes / (ms * 1e-3) / 1e9
+    value = job_value(world, grad_bytes, ms)
 
     # dominant group: the largest share of the step
     dom = max(group_ms, key=group_ms.get)
@@ -389,8 +406,8 @@ def main_gift(args):
 
     # ---- end to end through the public API with host buffers --------------------------
     e2e = None
-    if not args.no_e2e and rank == 0:
-        e2e = run_e2e(args, G, ctx, gl, eu, factors, R, wss[0], st, graphs, dev, grad_bytes)
+    if not args.no_e2e:
+        e2e = run_e2e(args, gl, eu, graphs, dev, grad_bytes, world)
 
     # ---- CPU baseline (oracle on a bounded sample) --------------------------------------
     cpu = None
@@ -423,10 +440,10 @@ def main_gift(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes):
+def run_e2e(args, gl, eu, graphs, dev, grad_bytes, world):
     """Same step through the public API with host buffers: per step, copy every replica
     gradient from pinned host memory, run the codec, read the decoded / averaged results
-    back to pinned host memory."""
+    back to pinned host memory.  Every rank does this; the slowest rank's time counts."""
     import torch
     host_in, dev_in = [], []
     for L in gl + eu:
@@ -442,6 +459,9 @@ def run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes):
     torch.cuda.synchronize()
     steps = max(1, args.e2e_steps)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     t0.record()
     for _ in range(steps):
         for h, d in zip(host_in, dev_in):
@@ -452,8 +472,10 @@ def run_e2e(args, G, ctx, gl, eu, factors, R, ws, st, graphs, dev, grad_bytes):
             h.copy_(o, non_blocking=True)
     t1.record()
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    return {"value": grad_bytes / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / steps
+    return {"value": job_value(world, grad_bytes, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
 
 

@@ -46,6 +46,7 @@ int lr_proj_splits(int sms, int d_out, int d_in);
 cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in, const float *U, int rank,
                            float *part, int nsplit);
 // Pc[row][k] = c_k * sum_s part[s][row][k]; c from (mu, sigma), inverse = map-back coefficients.
+// pc_terms (nullable): also the BF16 term planes of Pc for the tensor-core apply.
 cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
                                const float *sigma, int rank, bool inverse, float *Pc, float *pc_terms = nullptr,
                                int terms = 3);
@@ -67,8 +68,9 @@ struct LrApply {
   float *tscale;
   float *amax_out;
   float *out;               // LR_STORE
-  int terms;                // tensor-core path: 1 = one TF32 product (TC), otherwise 3-term split (FP32)
-  float *split;             // TF32 term planes: Pc terms (3 x d_out x 32) then U terms (3 x d_in x 32)
+  int terms;                // tensor-core path: 1 = TC precision (two BF16 terms, three products),
+                            // otherwise FP32 precision (three BF16 terms, six products)
+  float *split;             // BF16 term planes (tc.cuh): Pc planes (2 x d_out x 32 floats), then U
 };
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
 // lowrank_tc.cu: the same apply on tcgen05 tensor cores (vectorised shapes only)

@@ -13,6 +13,7 @@
 //   k_lr_apply     V = alpha X + Pc U^T on a 2-D tile, fused with its consumer: amax, FP8
 //                  pack (per tensor or per 128 x 128 block), NVFP4 pack, or FP32 store.
 #include "kernels.cuh"
+#include "tc.cuh"
 
 namespace gift {
 
@@ -183,16 +184,9 @@ __global__ void __launch_bounds__(256) k_lr_finalize(const float *__restrict__ p
   const float pc = (float)(coef[idx & 31] * ((double)s - (double)comp));
   Pc[idx] = pc;
   if (pc_terms) {
-    // exact TF32 terms pc = t1 + t2 + t3 (each with its low 13 mantissa bits zero) for the
-    // tensor-core apply; plane q at pc_terms + q * d_out * 32
-    const float t1 = __uint_as_float((__float_as_uint(pc) + 0x1000u) & 0xFFFFE000u);
-    const float r1 = pc - t1;
-    const float t2 = __uint_as_float((__float_as_uint(r1) + 0x1000u) & 0xFFFFE000u);
-    pc_terms[idx] = t1;
-    if (terms > 1) {
-      pc_terms[(size_t)d_out * 32 + idx] = t2;
-      pc_terms[(size_t)2 * d_out * 32 + idx] = r1 - t2;
-    }
+    // BF16 term planes of Pc for the tensor-core apply (1 plane: TC path, 2: FP32 path)
+    tc::write_term_planes(reinterpret_cast<uint16_t *>(pc_terms), (size_t)d_out, (size_t)(idx >> 5), idx & 31, pc,
+                          terms == 1 ? 1 : 2);
   }
 }
 

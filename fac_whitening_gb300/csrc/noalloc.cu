@@ -9,7 +9,7 @@
 // that scratch in one fixed array in device memory that the library itself declares, so
 // the call allocates nothing at all.
 //
-// The array (about 16 MiB) exists on every GPU that loads the library, for as long as the
+// The array (about 14 MiB) exists on every GPU that loads the library, for as long as the
 // process lives.  All calls on a device share it: two calls whose work overlaps on the GPU
 // (different streams without ordering between them) race on it and give wrong results, so
 // order them on one stream or with events.  The amax word is cleared by every call; the
@@ -29,7 +29,7 @@ constexpr int kNoAllocMaxCols = 16384;                       // d_in limit
 constexpr size_t kNoAllocAmaxFloats = 64;                    // one word, padded to 256 B
 constexpr size_t kNoAllocPcFloats = (size_t)kNoAllocMaxRows * 32;
 constexpr size_t kNoAllocPartFloats = (size_t)2 << 20;       // 8 MiB of projection partials
-constexpr size_t kNoAllocSplitFloats = (size_t)3 * 32 * (kNoAllocMaxRows + kNoAllocMaxCols);   // 7.5 MiB
+constexpr size_t kNoAllocSplitFloats = (size_t)2 * 32 * (kNoAllocMaxRows + kNoAllocMaxCols);   // 5 MiB
 constexpr size_t kNoAllocFloats = kNoAllocAmaxFloats + kNoAllocPcFloats + kNoAllocPartFloats + kNoAllocSplitFloats;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace gift {
 namespace tc {
@@ -81,6 +82,47 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor: D = F32, A = B = BF16 (kind::f16), both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 BF16 step; issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, one 128 x N x 16 BF16 step with A in tensor memory
+// (lane m = row m of A, each 32-bit column holds two consecutive K elements, the lower K in the
+// low half); issued by one thread.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Registers -> 16 consecutive 32-bit columns of this thread's lane (a warp writes its
+// 32-lane slice); tmem_wait_st before the data is used by another agent.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 // D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 8 TF32 step; issued by one thread.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -100,8 +142,18 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 // ---- TMEM -> registers ----------------------------------------------------------------------
 // 32 consecutive 32-bit columns of this thread's lane (a warp reads its 32-lane slice).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r);
+__device__ __forceinline__ void tmem_wait_ld(uint32_t *r);
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
+  tmem_ld32_nowait(taddr, r);
+  tmem_wait_ld(r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive columns without the completion wait (tmem_wait_ld before using v).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -111,9 +163,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Completion wait for tmem_ld32_nowait; the registers pass through it so that no use of them
+// can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t *r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// ---- exact BF16 splitting ------------------------------------------------------------------
+// x = t1 + t2 + t3 with each term a BF16 value (round to nearest at every step).  BF16 keeps
+// FP32's exponent range, so each remainder is formed exactly (the operands of each
+// subtraction are within a factor of two) and 8 + 8 + 8 significant bits cover the 24 of x:
+// the last remainder fits in BF16 exactly (values below 2^-110 aside, where BF16 subnormals
+// drop bits worth less than 2^-133).
+__device__ __forceinline__ void bf16_split3(float x, uint16_t &t1, uint16_t &t2, uint16_t &t3) {
+  const __nv_bfloat16 h1 = __float2bfloat16_rn(x);
+  const float r1 = __fsub_rn(x, __bfloat162float(h1));
+  const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+  const float r2 = __fsub_rn(r1, __bfloat162float(h2));
+  const __nv_bfloat16 h3 = __float2bfloat16_rn(r2);
+  t1 = __bfloat16_as_ushort(h1);
+  t2 = __bfloat16_as_ushort(h2);
+  t3 = __bfloat16_as_ushort(h3);
+}
+// Operand planes of the tensor-core apply, for element (row, k < 32) of a rows x 32 operand:
+// plane 0 row = [t1 of k = 0..31 | t2 of k = 0..31] (128 bytes), plane 1 row = [t3 | zeros].
+// `planes` holds nplanes planes of rows x 64 BF16 each.
+__device__ __forceinline__ void write_term_planes(uint16_t *planes, size_t rows, size_t row, int k, float x,
+                                                  int nplanes) {
+  uint16_t t1, t2, t3;
+  bf16_split3(x, t1, t2, t3);
+  uint16_t *p0 = planes + row * 64;
+  p0[k] = t1;
+  p0[32 + k] = t2;
+  if (nplanes > 1) {
+    uint16_t *p1 = planes + rows * 64 + row * 64;
+    p1[k] = t3;
+    p1[32 + k] = 0;
+  }
 }
 
 // ---- exact TF32 splitting -----------------------------------------------------------------

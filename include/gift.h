@@ -96,9 +96,12 @@ typedef enum {
   GIFT_XF_CHOL_TWO_SIDED = 3
 } gift_xform;
 
-/* Arithmetic of the transforms.  FP32: FP32 arithmetic, relative Frobenius error of
- * the transformed and decoded tensors within 1e-5 of exact.  TC: reduced-precision
- * tensor-core arithmetic, within 2e-2 (accepted; currently runs the FP32 path). */
+/* Arithmetic of the transforms.  FP32: results within FP32 rounding, the transformed and
+ * decoded tensors within 1e-5 (relative Frobenius) of exact.  Where the rank-r product runs on
+ * the tensor cores (rank-r transforms with d_in % 32 == 0 and 16-byte aligned tensors), FP32
+ * splits Pc and U exactly into three BF16 terms and sums the six products with i + j <= 4
+ * (what is dropped is below 2^-23 of each |Pc_k U_k|).  TC: two terms and three products
+ * (below 2^-15), the transformed tensor within 2e-2; other transforms run the FP32 path. */
 typedef enum { GIFT_PREC_FP32 = 0, GIFT_PREC_TC = 1 } gift_precision;
 
 /* Element type of activation inputs. */
@@ -258,7 +261,7 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
  * per-tensor scaling, but without a caller workspace: for callers that cannot allocate
  * device memory at the point where they encode, such as code running inside a gradient or
  * communication hook while the framework's allocator must not grow, or C programs with no
- * allocator of their own.  Its scratch (about 16 MiB) is a fixed array inside the library,
+ * allocator of their own.  Its scratch (about 14 MiB) is a fixed array inside the library,
  * present on every GPU that loads it until the process exits.
  *  Limits: d_out <= 4096, d_in <= 16384, and the split-K projection partials must fit the scratch
  *  (ceil-split count x d_out x 32 floats <= 2^21); beyond them the call returns
