@@ -36,12 +36,12 @@ bool valid_kind(gift_xform k) { return k >= GIFT_XF_IDENTITY && k <= GIFT_XF_CHO
 
 // ---- codec workspace (encode / amax / decode) -----------------------------------------
 struct CodecWs {
-  float *amax = nullptr;   // one word (64 floats reserved)
+  float *amax = nullptr;   // amax word at [0], grid-barrier word at [16] (64 floats reserved)
   float *part = nullptr;   // LOWRANK: nsplit x d_out x 32 slice partials of X U
   float *Pc = nullptr;     // LOWRANK: d_out x 32
   float *xbuf = nullptr;   // transformed tensor (CHOL encode) or dequantised input (decode)
   float *tbuf = nullptr;   // CHOL_TWO_SIDED intermediate
-  float *split = nullptr;  // LOWRANK: TF32 term planes for the tensor-core apply
+  float *split = nullptr;  // LOWRANK: tensor-core operand planes and counters (kernels.cuh)
   int nsplit = 0;
   size_t bytes = 0;
 };
@@ -53,7 +53,7 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
   w.amax = c.take<float>(64);
   if (kind == GIFT_XF_LOWRANK) {
     w.nsplit = lr_proj_splits(sms, d_out, d_in);
-    w.part = c.take<float>((size_t)w.nsplit * d_out * 32);
+    w.part = c.take<float>(lr_part_floats(sms, d_out, d_in));
     w.Pc = c.take<float>((size_t)d_out * 32);
     w.split = c.take<float>(lr_pipe_split_floats(d_out, d_in));
   }
@@ -210,24 +210,12 @@ LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const
   return a;
 }
 
-// Projection and coefficients; for shapes the tensor-core apply takes, also the TF32 term
-// planes of Pc (by the finalize) and of U.
+// Projection and coefficients; for shapes the tensor-core kernels take, also their operand
+// planes.
 cudaError_t lr_prepare(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w,
                        bool inverse, gift_precision prec) {
-  cudaError_t e = launch_lr_proj(L, X, d_out, d_in, f->U, f->rank, w.part, w.nsplit);
-  if (e != cudaSuccess) return e;
-  const int terms = (prec == GIFT_PREC_TC) ? 1 : 3;
-  float *pc_terms = (d_in % 32 == 0) ? w.split : nullptr;
-  e = launch_lr_finalize(L, w.part, w.nsplit, d_out, f->mu, f->sigma, f->rank, inverse, w.Pc, pc_terms, terms);
-  if (e != cudaSuccess || !pc_terms) return e;
-  LrApply a{};
-  a.U = f->U;
-  a.rank = f->rank;
-  a.d_out = d_out;
-  a.d_in = d_in;
-  a.terms = terms;
-  a.split = w.split;
-  return launch_lr_split_u(L, a);
+  return lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, X, d_out, d_in, inverse, prec == GIFT_PREC_TC, w.part,
+                        w.Pc, (d_in % 32 == 0) ? w.split : nullptr);
 }
 
 }  // namespace
@@ -506,15 +494,22 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
       CK(launch_lr_apply(L, LR_BLOCK, fmt, a));
       return GIFT_OK;
     }
+    const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
+    if (!amax_in) CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
+    a.amax_ws = w.amax;
+    a.grid_counter = reinterpret_cast<unsigned int *>(w.amax + 16);
+    if (lr_encode_fused_ok(L, a, epi)) {
+      // one pass over W: transform, grid-wide amax and pack with W~ held on chip
+      CK(cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream));
+      CK(launch_lr_encode_fused(L, epi, fmt, a));
+      return GIFT_OK;
+    }
     if (!amax_in) {
-      CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
       LrApply am = a;
       am.tout = nullptr;
-      am.amax_ws = w.amax;
       CK(launch_lr_apply(L, LR_AMAX, fmt, am));
     }
-    a.amax_ws = w.amax;
-    CK(launch_lr_apply(L, fmt == GIFT_FMT_NVFP4 ? LR_NVFP4 : LR_PACK_TENSOR, fmt, a));
+    CK(launch_lr_apply(L, epi, fmt, a));
     return GIFT_OK;
   }
 

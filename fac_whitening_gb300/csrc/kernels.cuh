@@ -50,6 +50,13 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
 cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
                                const float *sigma, int rank, bool inverse, float *Pc, float *pc_terms = nullptr,
                                int terms = 3);
+// Everything the apply needs before it runs: P = X U, Pc and, when `split` is given and the
+// shape allows, the tensor-core operand planes (tensor-core projection where eligible,
+// otherwise the FP32-SIMT projection and finalize).  `part` holds lr_part_floats floats.
+cudaError_t lr_prepare_all(const Launch &L, const float *U, const float *mu, const float *sigma, int rank,
+                           const float *X, int d_out, int d_in, bool inverse, bool tc_precision, float *part,
+                           float *Pc, float *split);
+size_t lr_part_floats(int sms, int d_out, int d_in);
 // Fused apply V = alpha X + Pc U^T (+ R), alpha = sigma^-1/2 (or sigma^1/2 for the map back).
 enum LrEpi { LR_AMAX = 0, LR_PACK_TENSOR = 1, LR_BLOCK = 2, LR_NVFP4 = 3, LR_STORE = 4, LR_BLOCK_AMAX = 5 };
 struct LrApply {
@@ -71,6 +78,7 @@ struct LrApply {
   int terms;                // tensor-core path: 1 = TC precision (two BF16 terms, three products),
                             // otherwise FP32 precision (three BF16 terms, six products)
   float *split;             // BF16 term planes (tc.cuh): Pc planes (2 x d_out x 32 floats), then U
+  unsigned int *grid_counter;   // fused encode: grid-barrier word, zero before the launch
 };
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
 // lowrank_tc.cu: the same apply on tcgen05 tensor cores (vectorised shapes only)
@@ -78,6 +86,28 @@ bool lr_apply_tc_ok(const LrApply &a, int epi);
 size_t lr_pipe_split_floats(int d_out, int d_in);
 cudaError_t launch_lr_split_u(const Launch &L, const LrApply &a);
 cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply &a, bool single_term);
+// Fused encode (transform, grid-wide amax, pack; W read once) for per-tensor FP8 and NVFP4
+// on shapes whose tiles fit in tensor memory across the SMs; cooperative launch.
+bool lr_encode_fused_ok(const Launch &L, const LrApply &a, int epi);
+cudaError_t launch_lr_encode_fused(const Launch &L, int epi, int fmt, const LrApply &a);
+// lowrank_proj_tc.cu: the projection and the finalize on the tensor cores.  The tensor-core
+// workspace ("split", lr_pipe_split_floats floats) holds, in order: the Pc term planes
+// (2 x d_out rows of 64 BF16), the U term planes for the apply (2 x d_in rows), the U^T term
+// planes for the projection (3 x 32 rows of d_in BF16) and one counter per 128-row block.
+struct LrPlanes {
+  uint16_t *pc, *u, *ut;
+  unsigned int *counters;
+  int ncounters;
+};
+LrPlanes lr_planes(float *split, int d_out, int d_in);
+int lr_proj_tc_splits(int sms, int d_out, int d_in);
+bool lr_proj_tc_ok(const float *X, int d_in, const float *split);
+// U planes in both layouts (and the counters zeroed); then P, Pc and the Pc planes.
+cudaError_t launch_lr_split_u_all(const Launch &L, const float *U, int d_out, int d_in, int rank, int nplanes_apply,
+                                  float *split);
+cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_in, const float *mu,
+                              const float *sigma, int rank, bool inverse, bool tc_precision, float *part, float *Pc,
+                              float *split);
 
 // Sets a kernel's opt-in dynamic shared-memory size once per device and kernel (so no
 // attribute call happens inside a stream capture after the first eager call).  Keyed on the

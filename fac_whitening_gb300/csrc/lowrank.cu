@@ -455,6 +455,38 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
   return cudaGetLastError();
 }
 
+cudaError_t lr_prepare_all(const Launch &L, const float *U, const float *mu, const float *sigma, int rank,
+                           const float *X, int d_out, int d_in, bool inverse, bool tc_precision, float *part,
+                           float *Pc, float *split) {
+  cudaError_t e;
+  if (split && lr_proj_tc_ok(X, d_in, split)) {
+    if ((e = launch_lr_split_u_all(L, U, d_out, d_in, rank, tc_precision ? 1 : 2, split)) != cudaSuccess) return e;
+    return launch_lr_proj_tc(L, X, d_out, d_in, mu, sigma, rank, inverse, tc_precision, part, Pc, split);
+  }
+  const int nsplit = lr_proj_splits(L.sms, d_out, d_in);
+  if ((e = launch_lr_proj(L, X, d_out, d_in, U, rank, part, nsplit)) != cudaSuccess) return e;
+  float *pc_terms = (split && d_in % 32 == 0) ? split : nullptr;
+  const int terms = tc_precision ? 1 : 3;
+  if ((e = launch_lr_finalize(L, part, nsplit, d_out, mu, sigma, rank, inverse, Pc, pc_terms, terms)) != cudaSuccess)
+    return e;
+  if (!pc_terms) return cudaSuccess;
+  LrApply a{};
+  a.U = U;
+  a.rank = rank;
+  a.d_out = d_out;
+  a.d_in = d_in;
+  a.terms = terms;
+  a.split = split;
+  return launch_lr_split_u(L, a);
+}
+
+size_t lr_part_floats(int sms, int d_out, int d_in) {
+  int ns = lr_proj_splits(sms, d_out, d_in);
+  const int nt = lr_proj_tc_splits(sms, d_out, d_in);
+  if (nt > ns) ns = nt;
+  return (size_t)ns * d_out * 32;
+}
+
 cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, int d_out, const float *mu,
                                const float *sigma, int rank, bool inverse, float *Pc, float *pc_terms, int terms) {
   const int n = d_out * 32;

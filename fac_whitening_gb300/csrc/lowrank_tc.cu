@@ -301,8 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
             *reinterpret_cast<float4 *>(dst + (size_t)gr * d_in + gc) =
                 *reinterpret_cast<const float4 *>(st + (c16 >> 3) * kWBox + sw128(rr, c16 & 7));
         }
-        // this warp's generic-proxy writes into the stage are ordered before the TMA refill
-        tc::fence_proxy_async_smem();
       }
       if (EPI == LR_PACK_TENSOR) {
         uint32_t w4[8];
@@ -341,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
                                         (c0 + 32 * half) / kNvGroup) = sc;
         }
       }
+      // this warp's generic-proxy reads (and writes) of the stage are ordered before the
+      // async-proxy (TMA) refill
+      tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar_empty[s]);
     }
@@ -362,6 +363,303 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// =========================================================================================
+// Fused encode: transform, grid-wide amax and pack with W~ held in tensor memory.
+//
+// Each CTA owns at most kSlots tiles of one row block and keeps every tile's W~ in its own
+// 64-column TMEM slot (8 slots = all 512 columns), so W is read from HBM once: phase A runs
+// the pipeline above (A = Pc term planes from shared memory, loaded once; B = U planes and W
+// streamed per tile), forms W~ = alpha W + Pc U^T, folds it into the CTA amax and writes it
+// back into the slot; the CTAs then meet at one grid-wide barrier (launched cooperatively, so
+// all CTAs are resident; the wait is clock-bounded) after which every CTA reads the tensor
+// amax and packs its tiles straight out of tensor memory (phase B).  With a caller-supplied
+// amax there is no barrier.  The arithmetic of W~, the amax and the codes is the same as in
+// the two-kernel path (amax pass, then pack pass).
+// =========================================================================================
+namespace {
+
+constexpr int kSlots = 8;
+constexpr int kAPlaneF = 128 * 128;   // Pc plane in shared memory: 128 rows x 128 bytes
+
+struct FusedParams {
+  LrApply a;
+  int tiles_n;
+  int cpr;
+  unsigned int *grid_counter;   // zero on entry
+};
+
+template <int NPL>
+struct FLayout {
+  static constexpr int stage_bytes = 2 * kWBox + NPL * kBPlane;
+  static constexpr int stage_off = NPL * kAPlaneF;
+  static constexpr int total = stage_off + kStages * stage_bytes;
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+}  // namespace
+
+template <int EPI, int F, int NPL, bool TOUT>
+__global__ void __launch_bounds__(kThreads, 1) k_lr_encode_fused(const __grid_constant__ FusedParams P,
+                                                                 const __grid_constant__ CUtensorMap tmW,
+                                                                 const __grid_constant__ CUtensorMap tmA,
+                                                                 const __grid_constant__ CUtensorMap tmB, int *status) {
+  using Lay = FLayout<NPL>;
+  extern __shared__ uint8_t dsm[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_tfull[kSlots], bar_afull;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ uint32_t red[kReadWarps];
+  __shared__ float amax_sh;
+  __shared__ volatile int failed;
+
+  const LrApply &a = P.a;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d_out = a.d_out, d_in = a.d_in;
+  const int b = blockIdx.x;
+  const int rb = b / P.cpr, jc = b - rb * P.cpr;
+  const int t_begin = rb * P.tiles_n + (int)(((long long)P.tiles_n * jc) / P.cpr);
+  const int t_end = rb * P.tiles_n + (int)(((long long)P.tiles_n * (jc + 1)) / P.cpr);
+  const int r0 = rb * kTileM;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base_sh, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&bar_full[s], 1);
+      tc::mbar_init(&bar_empty[s], kReadWarps);
+    }
+    for (int s = 0; s < kSlots; ++s) tc::mbar_init(&bar_tfull[s], 1);
+    tc::mbar_init(&bar_afull, 1);
+    tc::fence_mbar_init();
+    failed = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+
+  auto wait = [&](uint64_t *bar, uint32_t parity) {
+    if (failed) return false;
+    if (!tc::mbar_wait_bounded(bar, parity, kWaitBudget)) {
+      failed = 1;
+      set_status(status, GIFT_ERR_TIMEOUT);
+      return false;
+    }
+    return true;
+  };
+
+  if (warp == kReadWarps) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued[kStages] = {};
+      bool a_issued = false;
+      if (t_end > t_begin) {
+        tc::mbar_arrive_expect_tx(&bar_afull, NPL * kAPlaneF);
+#pragma unroll
+        for (int q = 0; q < NPL; ++q) tc::tma_load_2d(sm + q * kAPlaneF, &tmA, 0, q * d_out + r0, &bar_afull);
+        a_issued = true;
+      }
+      for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+        const int cb = t - rb * P.tiles_n;
+        const int s = i % kStages;
+        if (!wait(&bar_empty[s], ((i / kStages) & 1) ^ 1)) break;
+        uint8_t *st = sm + Lay::stage_off + s * Lay::stage_bytes;
+        tc::mbar_arrive_expect_tx(&bar_full[s], Lay::stage_bytes);
+        tc::tma_load_2d(st, &tmW, cb * kTileN, r0, &bar_full[s]);
+        tc::tma_load_2d(st + kWBox, &tmW, cb * kTileN + 32, r0, &bar_full[s]);
+#pragma unroll
+        for (int q = 0; q < NPL; ++q)
+          tc::tma_load_2d(st + 2 * kWBox + q * kBPlane, &tmB, 0, q * d_in + cb * kTileN, &bar_full[s]);
+        ++issued[s];
+      }
+      if (failed) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) tc::mbar_wait_bounded(&bar_full[s], (uint32_t)((issued[s] - 1) & 1), kWaitBudget);
+        if (a_issued) tc::mbar_wait_bounded(&bar_afull, 0, kWaitBudget);
+      }
+    }
+  } else if (warp == kReadWarps + 1) {
+    // ---------------- MMA issuer: one TMEM slot per tile ----------------
+    if (lane == 0 && t_end > t_begin) {
+      constexpr uint32_t idesc = tc::idesc_bf16(kTileM, kTileN);
+      constexpr int np = (NPL == 1) ? 3 : 6;
+      constexpr int pa[6] = {NPL == 1 ? 1 : 2, NPL == 1 ? 0 : 1, 0, 1, 0, 0};
+      constexpr int pb[6] = {0, 1, NPL == 1 ? 0 : 2, 0, 1, 0};
+      if (wait(&bar_afull, 0)) {
+        const uint32_t a0 = tc::smem_u32(sm);
+        for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+          const int s = i % kStages;
+          if (!wait(&bar_full[s], (uint32_t)((i / kStages) & 1))) break;
+          tc::fence_after_sync();
+          const uint32_t b0 = tc::smem_u32(sm + Lay::stage_off + s * Lay::stage_bytes + 2 * kWBox);
+          uint32_t acc = 0;
+#pragma unroll
+          for (int p = 0; p < np; ++p) {
+            const uint32_t aa = a0 + (pa[p] >> 1) * kAPlaneF + 64 * (pa[p] & 1);
+            const uint32_t bb = b0 + (pb[p] >> 1) * kBPlane + 64 * (pb[p] & 1);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              tc::mma_bf16(tmem + (uint32_t)(i * kTileN), tc::sdesc_kmajor_sw128(aa + 32 * k),
+                           tc::sdesc_kmajor_sw128(bb + 32 * k), idesc, acc);
+              acc = 1;
+            }
+          }
+          tc::mma_commit(&bar_tfull[i]);
+        }
+      }
+    }
+  } else {
+    // ---------------- read-out (warps 0-7): thread = one tile row, 32 columns ----------------
+    const int quarter = warp & 3, half = warp >> 2;
+    const double sg = (double)a.sigma[0];
+    const float alpha = a.inverse ? (float)sqrt(sg) : (float)(1.0 / sqrt(sg));
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int lr = quarter * 32 + lane;
+    const int row = r0 + lr;
+    uint32_t m_run = 0;
+    // phase A: W~ of every tile into its slot, CTA amax
+    for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+      const int cb = t - rb * P.tiles_n, c0 = cb * kTileN;
+      const int s = i % kStages;
+      wait(&bar_tfull[i], 0);
+      wait(&bar_full[s], (uint32_t)((i / kStages) & 1));
+      tc::fence_after_sync();
+      const uint32_t slot = tmem + lane_off + (uint32_t)(i * kTileN + 32 * half);
+      uint32_t raw[32];
+      tc::tmem_ld32_nowait(slot, raw);
+      const uint8_t *box = sm + Lay::stage_off + s * Lay::stage_bytes + half * kWBox;
+      float4 w[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const float4 *>(box + sw128(lr, c));
+      tc::tmem_wait_ld(raw);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        raw[4 * c + 0] = __float_as_uint(fmaf(alpha, w[c].x, __uint_as_float(raw[4 * c + 0])));
+        raw[4 * c + 1] = __float_as_uint(fmaf(alpha, w[c].y, __uint_as_float(raw[4 * c + 1])));
+        raw[4 * c + 2] = __float_as_uint(fmaf(alpha, w[c].z, __uint_as_float(raw[4 * c + 2])));
+        raw[4 * c + 3] = __float_as_uint(fmaf(alpha, w[c].w, __uint_as_float(raw[4 * c + 3])));
+      }
+      // W was read through the generic proxy and the refill writes through the async (TMA)
+      // proxy: order the reads before the hand-back
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_empty[s]);
+      const bool in = row < d_out && (c0 + 32 * half) < d_in;
+      if (in) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) m_run = max(m_run, raw[e] & 0x7FFFFFFFu);
+        if (TOUT) {
+          float4 *dst = reinterpret_cast<float4 *>(a.tout + (size_t)row * d_in + c0 + 32 * half);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_float4(__uint_as_float(raw[4 * c]), __uint_as_float(raw[4 * c + 1]),
+                                 __uint_as_float(raw[4 * c + 2]), __uint_as_float(raw[4 * c + 3]));
+        }
+      }
+      tc::tmem_st16(slot, raw);
+      tc::tmem_st16(slot + 16, raw + 16);
+      tc::tmem_wait_st();
+    }
+    // CTA amax, then (without a caller amax) the grid-wide maximum
+    m_run = warp_max_u32(m_run);
+    if (lane == 0) red[warp] = m_run;
+    tc::named_bar_sync(1, 32 * kReadWarps);
+    if (tid == 0) {
+      uint32_t m = 0;
+      for (int w = 0; w < kReadWarps; ++w) m = max(m, red[w]);
+      float amax;
+      if (a.amax_in) {
+        amax = a.amax_in[0];
+      } else {
+        if (m) atomicMax(reinterpret_cast<uint32_t *>(a.amax_ws), m);
+        __threadfence();
+        atomicAdd(P.grid_counter, 1u);
+        const long long t0 = clock64();
+        while (ld_acquire_u32(P.grid_counter) < gridDim.x) {
+          if (clock64() - t0 > kWaitBudget) {
+            set_status(status, GIFT_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(64);
+        }
+        amax = __uint_as_float(ld_acquire_u32(reinterpret_cast<const unsigned int *>(a.amax_ws)));
+      }
+      amax_sh = amax;
+      if (b == 0) {
+        if (!(amax <= kF32Max)) set_status(status, GIFT_ERR_NONFINITE);
+        if (EPI == LR_PACK_TENSOR) reinterpret_cast<float *>(a.scales)[0] = scale_pair(amax, fmax_of<F>()).s;
+        else a.tscale[0] = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, kNvfp4TensorDiv);
+        if (a.amax_out) a.amax_out[0] = amax;
+      }
+    }
+    tc::named_bar_sync(1, 32 * kReadWarps);
+    const float amax = amax_sh;
+    const ScalePair sp = scale_pair(amax, fmax_of<F>());
+    const float s_t = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, kNvfp4TensorDiv);
+    // phase B: pack every tile out of its slot
+    for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+      const int cb = t - rb * P.tiles_n, c0 = cb * kTileN;
+      uint32_t raw[32];
+      tc::tmem_ld32_nowait(tmem + lane_off + (uint32_t)(i * kTileN + 32 * half), raw);
+      tc::tmem_wait_ld(raw);
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[e]);
+      const bool in = row < d_out && (c0 + 32 * half) < d_in;
+      if (EPI == LR_PACK_TENSOR) {
+        uint32_t w4[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float *x = v + 4 * h;
+          w4[h] = pack4_fp8<F>(__fmul_rn(x[0], sp.m), __fmul_rn(x[1], sp.m), __fmul_rn(x[2], sp.m),
+                               __fmul_rn(x[3], sp.m));
+        }
+        if (in) {
+          uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (size_t)row * d_in + c0 + 32 * half);
+          dst[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          dst[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+        }
+      } else {
+        uint16_t sc = 0;
+        uint32_t cw[4];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t gm = 0;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) gm = max(gm, abs_bits(v[16 * g + e]));
+          const Nv4Group grp = nvfp4_group(__uint_as_float(gm), s_t);
+          float y[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) y[e] = __fmul_rn(v[16 * g + e], grp.r);
+          cw[2 * g] = pack8_e2m1(y);
+          cw[2 * g + 1] = pack8_e2m1(y + 8);
+          sc |= (uint16_t)grp.e_code << (8 * g);
+        }
+        if (in) {
+          *reinterpret_cast<uint4 *>(a.codes + (((size_t)row * d_in + c0 + 32 * half) >> 1)) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(a.scales) + (size_t)row * (d_in / kNvGroup) +
+                                        (c0 + 32 * half) / kNvGroup) = sc;
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -413,9 +711,12 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 
 }  // namespace
 
-// Term-plane workspace: up to two planes of 32 floats (64 BF16) per row for Pc (d_out rows),
-// then the same for U (d_in rows).
-size_t lr_pipe_split_floats(int d_out, int d_in) { return (size_t)2 * 32 * ((size_t)d_out + d_in); }
+// Tensor-core workspace: Pc planes, U planes (the apply), U^T planes (the projection) and the
+// projection's row-block counters (see kernels.cuh).
+size_t lr_pipe_split_floats(int d_out, int d_in) {
+  const size_t blocks = ((size_t)d_out + 127) / 128;
+  return (size_t)64 * ((size_t)d_out + d_in) + (size_t)48 * d_in + ((blocks + 63) / 64) * 64;
+}
 
 // The pipelined apply covers the per-tensor FP8, NVFP4, amax and store epilogues with
 // d_in % 32 == 0 (TMA boxes of 32 columns, 16-byte aligned rows), 16-byte aligned tensors,
@@ -490,6 +791,81 @@ static cudaError_t pipe_dispatch(const Launch &L, int epi, int fmt, const LrAppl
                                   : pipe_launch<LR_PACK_TENSOR, FMT_E4M3, NPL>(L, a);
   }
   return cudaErrorInvalidValue;
+}
+
+// Fused encode plan: CTAs per row block so that no CTA has more than kSlots tiles, all CTAs
+// resident at once (one per SM).  Returns the grid size, 0 if the shape does not fit.
+static int fused_plan(const Launch &L, const LrApply &a, int *cpr_out) {
+  const int tiles_n = (a.d_in + kTileN - 1) / kTileN;
+  const int tiles_m = (a.d_out + kTileM - 1) / kTileM;
+  if (tiles_m > L.sms) return 0;
+  int cpr = (tiles_n + kSlots - 1) / kSlots;
+  const int spread = L.sms / tiles_m;
+  if (spread > cpr) cpr = spread < tiles_n ? spread : tiles_n;
+  if ((long long)cpr * tiles_m > L.sms) return 0;
+  *cpr_out = cpr;
+  return cpr * tiles_m;
+}
+
+bool lr_encode_fused_ok(const Launch &L, const LrApply &a, int epi) {
+  if (epi != LR_PACK_TENSOR && epi != LR_NVFP4) return false;
+  if (!lr_apply_tc_ok(a, epi) || !a.grid_counter) return false;
+  int cpr = 0;
+  return fused_plan(L, a, &cpr) > 0;
+}
+
+template <int EPI, int F, int NPL, bool TOUT>
+static cudaError_t fused_launch(const Launch &L, const LrApply &a, int grid, int cpr) {
+  CUtensorMap tmW, tmA, tmB;
+  const float *pc = a.split;
+  const float *ut = a.split + (size_t)2 * 32 * a.d_out;
+  if (!make_map(&tmW, a.X, (uint64_t)a.d_out, (uint64_t)a.d_in, kTileM) ||
+      !make_map(&tmA, pc, (uint64_t)NPL * a.d_out, 32, kTileM) ||
+      !make_map(&tmB, ut, (uint64_t)NPL * a.d_in, 32, kTileN))
+    return cudaErrorInvalidValue;
+  FusedParams P;
+  P.a = a;
+  P.tiles_n = (a.d_in + kTileN - 1) / kTileN;
+  P.cpr = cpr;
+  P.grid_counter = a.grid_counter;
+  const int smem = FLayout<NPL>::total + 1024;
+  auto kern = k_lr_encode_fused<EPI, F, NPL, TOUT>;
+  cudaError_t e;
+  if ((e = ensure_dynamic_smem<k_lr_encode_fused<EPI, F, NPL, TOUT>>(smem)) != cudaSuccess) return e;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) != cudaSuccess) return e;
+  if (per_sm < 1 || grid > per_sm * L.sms) return cudaErrorCooperativeLaunchTooLarge;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P, tmW, tmA, tmB, L.status);
+}
+
+template <int NPL>
+static cudaError_t fused_dispatch(const Launch &L, int epi, int fmt, const LrApply &a, int grid, int cpr) {
+  if (epi == LR_NVFP4)
+    return a.tout ? fused_launch<LR_NVFP4, FMT_E4M3, NPL, true>(L, a, grid, cpr)
+                  : fused_launch<LR_NVFP4, FMT_E4M3, NPL, false>(L, a, grid, cpr);
+  if (fmt == GIFT_FMT_E5M2)
+    return a.tout ? fused_launch<LR_PACK_TENSOR, FMT_E5M2, NPL, true>(L, a, grid, cpr)
+                  : fused_launch<LR_PACK_TENSOR, FMT_E5M2, NPL, false>(L, a, grid, cpr);
+  return a.tout ? fused_launch<LR_PACK_TENSOR, FMT_E4M3, NPL, true>(L, a, grid, cpr)
+                : fused_launch<LR_PACK_TENSOR, FMT_E4M3, NPL, false>(L, a, grid, cpr);
+}
+
+// The caller has zeroed a.amax_ws (without a caller amax) and a.grid_counter on L.stream.
+cudaError_t launch_lr_encode_fused(const Launch &L, int epi, int fmt, const LrApply &a) {
+  int cpr = 0;
+  const int grid = fused_plan(L, a, &cpr);
+  if (grid <= 0) return cudaErrorInvalidValue;
+  return a.terms == 1 ? fused_dispatch<1>(L, epi, fmt, a, grid, cpr) : fused_dispatch<2>(L, epi, fmt, a, grid, cpr);
 }
 
 cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply &a, bool single_term) {

@@ -9,11 +9,11 @@
 // that scratch in one fixed array in device memory that the library itself declares, so
 // the call allocates nothing at all.
 //
-// The array (about 14 MiB) exists on every GPU that loads the library, for as long as the
+// The array (about 17 MiB) exists on every GPU that loads the library, for as long as the
 // process lives.  All calls on a device share it: two calls whose work overlaps on the GPU
 // (different streams without ordering between them) race on it and give wrong results, so
-// order them on one stream or with events.  The amax word is cleared by every call; the
-// other scratch is fully overwritten before it is read.
+// order them on one stream or with events.  The amax word and the grid-barrier word are
+// cleared by every call; the other scratch is fully overwritten before it is read.
 //
 // Set-up: the device address of the array is looked up once per device with
 // cudaGetSymbolAddress, on the first call made with that device current.  Make that first
@@ -29,7 +29,9 @@ constexpr int kNoAllocMaxCols = 16384;                       // d_in limit
 constexpr size_t kNoAllocAmaxFloats = 64;                    // one word, padded to 256 B
 constexpr size_t kNoAllocPcFloats = (size_t)kNoAllocMaxRows * 32;
 constexpr size_t kNoAllocPartFloats = (size_t)2 << 20;       // 8 MiB of projection partials
-constexpr size_t kNoAllocSplitFloats = (size_t)2 * 32 * (kNoAllocMaxRows + kNoAllocMaxCols);   // 5 MiB
+// tensor-core operand planes and counters (the lr_pipe_split_floats layout at the limits)
+constexpr size_t kNoAllocSplitFloats = (size_t)64 * (kNoAllocMaxRows + kNoAllocMaxCols) + (size_t)48 * kNoAllocMaxCols +
+                                       64;   // 8 MiB
 constexpr size_t kNoAllocFloats = kNoAllocAmaxFloats + kNoAllocPcFloats + kNoAllocPartFloats + kNoAllocSplitFloats;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
@@ -66,8 +68,8 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
     return GIFT_ERR_INVALID_ARG;
   // size limits of the fixed scratch
   if (d_out > kNoAllocMaxRows || d_in > kNoAllocMaxCols) return GIFT_ERR_INVALID_ARG;
-  const int nsplit = lr_proj_splits(ctx->sms, d_out, d_in);
-  if ((size_t)nsplit * d_out * 32 > kNoAllocPartFloats) return GIFT_ERR_INVALID_ARG;
+  if (lr_part_floats(ctx->sms, d_out, d_in) > kNoAllocPartFloats) return GIFT_ERR_INVALID_ARG;
+  if (lr_pipe_split_floats(d_out, d_in) > kNoAllocSplitFloats) return GIFT_ERR_INVALID_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != ctx->device || cur < 0 || cur >= kMaxDevices)
     return GIFT_ERR_INVALID_ARG;
@@ -86,9 +88,8 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   L.stream = stream;
   L.sms = ctx->sms;
   L.status = d_status;
-  if (launch_lr_proj(L, W, d_out, d_in, f->U, f->rank, part, nsplit) != cudaSuccess) return GIFT_ERR_CUDA;
-  float *pc_terms = (d_in % 32 == 0) ? split : nullptr;
-  if (launch_lr_finalize(L, part, nsplit, d_out, f->mu, f->sigma, f->rank, false, Pc, pc_terms, 3) != cudaSuccess)
+  float *planes = (d_in % 32 == 0) ? split : nullptr;
+  if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes) != cudaSuccess)
     return GIFT_ERR_CUDA;
   LrApply a{};
   a.X = W;
@@ -100,17 +101,20 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.d_in = d_in;
   a.inverse = false;
   a.terms = 3;
-  a.split = pc_terms;
-  if (pc_terms && launch_lr_split_u(L, a) != cudaSuccess) return GIFT_ERR_CUDA;
+  a.split = planes;
   a.codes = static_cast<uint8_t *>(codes);
   a.scales = scales;
   a.amax_out = amax_out;
   a.amax_in = amax_in;
   a.amax_ws = amax_ws;
-  if (!amax_in) {
-    if (cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
-    if (launch_lr_apply(L, LR_AMAX, fmt, a) != cudaSuccess) return GIFT_ERR_CUDA;
+  a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + 16);
+  if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
+  if (lr_encode_fused_ok(L, a, LR_PACK_TENSOR)) {
+    if (cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return GIFT_ERR_CUDA;
+    if (launch_lr_encode_fused(L, LR_PACK_TENSOR, fmt, a) != cudaSuccess) return GIFT_ERR_CUDA;
+    return GIFT_OK;
   }
+  if (!amax_in && launch_lr_apply(L, LR_AMAX, fmt, a) != cudaSuccess) return GIFT_ERR_CUDA;
   if (launch_lr_apply(L, LR_PACK_TENSOR, fmt, a) != cudaSuccess) return GIFT_ERR_CUDA;
   return GIFT_OK;
 }

@@ -177,6 +177,24 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t *r) {
                : "memory");
 }
 
+// 16 consecutive columns without the completion wait, and its wait.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t *r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+
 // ---- exact BF16 splitting ------------------------------------------------------------------
 // x = t1 + t2 + t3 with each term a BF16 value (round to nearest at every step).  BF16 keeps
 // FP32's exponent range, so each remainder is formed exactly (the operands of each
@@ -207,6 +225,35 @@ __device__ __forceinline__ void write_term_planes(uint16_t *planes, size_t rows,
     uint16_t *p1 = planes + rows * 64 + row * 64;
     p1[k] = t3;
     p1[32 + k] = 0;
+  }
+}
+
+// The same for 16 consecutive k (kb a multiple of 16), stored as 32-byte runs.
+__device__ __forceinline__ void write_term_planes16(uint16_t *planes, size_t rows, size_t row, int kb, const float *x,
+                                                    int nplanes) {
+  uint32_t w1[8], w2[8], w3[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint16_t a1, a2, a3, b1, b2, b3;
+    bf16_split3(x[2 * q], a1, a2, a3);
+    bf16_split3(x[2 * q + 1], b1, b2, b3);
+    w1[q] = (uint32_t)a1 | ((uint32_t)b1 << 16);
+    w2[q] = (uint32_t)a2 | ((uint32_t)b2 << 16);
+    w3[q] = (uint32_t)a3 | ((uint32_t)b3 << 16);
+  }
+  uint4 *p0 = reinterpret_cast<uint4 *>(planes + row * 64 + kb);
+  uint4 *p0b = reinterpret_cast<uint4 *>(planes + row * 64 + 32 + kb);
+  p0[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  p0[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+  p0b[0] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+  p0b[1] = make_uint4(w2[4], w2[5], w2[6], w2[7]);
+  if (nplanes > 1) {
+    uint4 *p1 = reinterpret_cast<uint4 *>(planes + rows * 64 + row * 64 + kb);
+    uint4 *p1b = reinterpret_cast<uint4 *>(planes + rows * 64 + row * 64 + 32 + kb);
+    p1[0] = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+    p1[1] = make_uint4(w3[4], w3[5], w3[6], w3[7]);
+    p1b[0] = make_uint4(0u, 0u, 0u, 0u);
+    p1b[1] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 

@@ -261,7 +261,7 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
  * per-tensor scaling, but without a caller workspace: for callers that cannot allocate
  * device memory at the point where they encode, such as code running inside a gradient or
  * communication hook while the framework's allocator must not grow, or C programs with no
- * allocator of their own.  Its scratch (about 14 MiB) is a fixed array inside the library,
+ * allocator of their own.  Its scratch (about 17 MiB) is a fixed array inside the library,
  * present on every GPU that loads it until the process exits.
  *  Limits: d_out <= 4096, d_in <= 16384, and the split-K projection partials must fit the scratch
  *  (ceil-split count x d_out x 32 floats <= 2^21); beyond them the call returns
