@@ -474,6 +474,26 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
   const bool block = (scaling == GIFT_SCALE_BLOCK128);
 
   if (kind == GIFT_XF_LOWRANK) {
+    if (fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && block) && !residual) {
+      // one pass over W where the shape fits on chip
+      LrApply o = lr_args(f, W, d_out, d_in, w, false, prec);
+      o.tout = transformed_out;
+      o.codes = c8;
+      o.scales = scales;
+      o.tscale = tensor_scale;
+      o.amax_out = amax_out;
+      o.amax_in = amax_in;
+      o.amax_ws = w.amax;
+      o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + 16);
+      const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
+      if (lr_encode_onepass_ok(L, o, epi, w.part, lr_part_floats(ctx->sms, d_out, d_in))) {
+        CK(launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split));
+        if (!amax_in) CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
+        CK(cudaMemsetAsync(o.grid_counter, 0, sizeof(unsigned int), stream));
+        CK(launch_lr_encode_onepass(L, epi, fmt, o, f->mu, w.part, w.Pc));
+        return GIFT_OK;
+      }
+    }
     CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = residual;

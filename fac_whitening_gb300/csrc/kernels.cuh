@@ -90,6 +90,12 @@ cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply 
 // on shapes whose tiles fit in tensor memory across the SMs; cooperative launch.
 bool lr_encode_fused_ok(const Launch &L, const LrApply &a, int epi);
 cudaError_t launch_lr_encode_fused(const Launch &L, int epi, int fmt, const LrApply &a);
+// lowrank_onepass.cu: projection, Pc, transform, grid-wide amax and pack in one cooperative
+// kernel (W read once).  Needs the U planes in a.split (launch_lr_split_u_all), a.amax_ws
+// zeroed (without a caller amax) and a.grid_counter zeroed.
+bool lr_encode_onepass_ok(const Launch &L, const LrApply &a, int epi, const float *part, size_t part_floats);
+cudaError_t launch_lr_encode_onepass(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
+                                     float *part, float *Pc);
 // lowrank_proj_tc.cu: the projection and the finalize on the tensor cores.  The tensor-core
 // workspace ("split", lr_pipe_split_floats floats) holds, in order: the Pc term planes
 // (2 x d_out rows of 64 BF16), the U term planes for the apply (2 x d_in rows), the U^T term

@@ -1,6 +1,6 @@
 // Rank-r projection P = X U on the 5th-generation tensor cores, split over K, with the
-// coefficient finalize (Pc = P diag(c), its BF16 term planes) fused into the last CTA of each
-// row block.
+// coefficient finalize (Pc = P diag(c), its BF16 term planes) fused in after a grid-wide
+// barrier.
 //
 // GIFT reading notes (zhongzhuzhou.org), simplification 2, eq. (17): the whitened gradient
 // is W~ = sigma^-1/2 W + ((W U) diag(c)) U^T, c = mu^-1/2 - sigma^-1/2; the map back uses
@@ -17,9 +17,10 @@
 // row and 32 K values); warp 9 issues the MMAs with A from tensor memory and B = U^T from
 // shared memory into a 128 x 32 FP32 accumulator per K tile (double-buffered), which the
 // splitter warps add up in registers with round-to-nearest FP32.  The partial P of the slice goes to
-// global memory; the last CTA of the row block to finish (counted with an atomic, no
-// waiting) sums the slices in slice order with a compensated FP32 sum, scales by c in FP64
-// and writes Pc and its term planes.  Every mbarrier wait is clock-bounded.
+// global memory; after one grid-wide barrier (the launch is cooperative when there is more
+// than one slice, so all CTAs are resident; the wait is clock-bounded) each CTA sums its share
+// of its row block's rows over the slices in slice order with a compensated FP32 sum, scales
+// by c in FP64 and writes Pc and its term planes.  Every mbarrier wait is clock-bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -51,8 +52,14 @@ struct ProjParams {
   float *Pc;               // d_out x 32
   uint16_t *pc_planes;     // term planes of Pc for the apply (pc_nplanes planes of d_out x 64 BF16)
   int pc_nplanes;
-  unsigned int *counters;  // one per row block, zero on entry, zero again on exit
+  unsigned int *counters;  // counters[0]: grid-barrier word, zero on entry
 };
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 template <int NT>
 struct PLayout {
@@ -72,7 +79,6 @@ __global__ void __launch_bounds__(kPThreads, 1) k_lr_proj_tc(const __grid_consta
   __shared__ uint64_t bar_full[kPStages], bar_empty[kPStages], bar_afull[2], bar_aempty[2], bar_cfull[2], bar_cempty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int failed;
-  __shared__ int is_last;
   __shared__ double coef[32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -99,6 +105,19 @@ __global__ void __launch_bounds__(kPThreads, 1) k_lr_proj_tc(const __grid_consta
     }
     tc::fence_mbar_init();
     failed = 0;
+  }
+  if (warp == 1) {   // FP64 coefficients of the finalize, off the critical path
+    const int k = lane;
+    double c = 0.0;
+    if (k < P.rank) {
+      const double m = (double)P.mu[k], sg = (double)P.sigma[0];
+      if (!(m > 0.0) || !(sg > 0.0)) {
+        if (blockIdx.x == 0) set_status(status, GIFT_ERR_NOT_PD);
+      } else {
+        c = P.inverse ? (sqrt(m) - sqrt(sg)) : (1.0 / sqrt(m) - 1.0 / sqrt(sg));
+      }
+    }
+    coef[k] = c;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -235,68 +254,57 @@ __global__ void __launch_bounds__(kPThreads, 1) k_lr_proj_tc(const __grid_consta
 #pragma unroll
       for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
-    // ---- last CTA of the row block: Pc = diag(c) sum of slices, and its term planes ----
+    // ---- Pc = diag(c) (sum of the slices), and its term planes ----
     __threadfence();
     tc::named_bar_sync(1, 32 * kPSplitWarps);
-    if (tid == 0) is_last = (atomicAdd(&P.counters[rb], 1u) == (unsigned)(P.nsplit - 1));
-    if (tid < 32) {
-      const int k = tid;
-      double c = 0.0;
-      if (k < P.rank) {
-        const double m = (double)P.mu[k], sg = (double)P.sigma[0];
-        if (!(m > 0.0) || !(sg > 0.0)) {
-          if (blockIdx.x == 0) set_status(status, GIFT_ERR_NOT_PD);
-        } else {
-          c = P.inverse ? (sqrt(m) - sqrt(sg)) : (1.0 / sqrt(m) - 1.0 / sqrt(sg));
+    if (P.nsplit > 1 && tid == 0) {
+      // grid-wide barrier (cooperative launch: every CTA is resident): all slices written
+      atomicAdd(P.counters, 1u);
+      const long long t0 = clock64();
+      while (ld_acquire_u32(P.counters) < gridDim.x) {
+        if (clock64() - t0 > kPWait) {
+          set_status(status, GIFT_ERR_TIMEOUT);
+          break;
         }
+        __nanosleep(64);
       }
-      coef[k] = c;
     }
     tc::named_bar_sync(1, 32 * kPSplitWarps);
-    if (is_last) {
-      __threadfence();
-      // thread = (row, 16 consecutive outputs); the slices are read four at a time (independent
-      // L2 loads in flight) and added in slice order with a compensated FP32 sum
-      const int rr = r0 + (tid >> 1), kb = 16 * (tid & 1);
-      if (rr < d_out) {
-        float sum[16], comp[16];
+    // this CTA's share of its row block; item = (row, 4 consecutive outputs).  The slices are
+    // read sixteen at a time (independent L2 loads in flight) and added in slice order with a
+    // compensated FP32 sum; the product with c is taken in FP64.
+    const int ra = r0 + (kPM * sp) / P.nsplit, rz = r0 + (kPM * (sp + 1)) / P.nsplit;
+    for (int item = tid; item < (rz - ra) * 8; item += 32 * kPSplitWarps) {
+      const int rr = ra + (item >> 3), kb = 4 * (item & 7);
+      if (rr >= d_out) continue;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f}, comp[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int q0 = 0; q0 < P.nsplit; q0 += 16) {
+        float4 x[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) sum[q] = comp[q] = 0.0f;
-        for (int q0 = 0; q0 < P.nsplit; q0 += 4) {
-          float4 x[4][4];
+        for (int u = 0; u < 16; ++u)
+          if (q0 + u < P.nsplit)
+            x[u] = __ldcg(reinterpret_cast<const float4 *>(P.part + ((size_t)(q0 + u) * d_out + rr) * 32 + kb));
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (q0 + u < P.nsplit) {
-              const float4 *src = reinterpret_cast<const float4 *>(P.part + ((size_t)(q0 + u) * d_out + rr) * 32 + kb);
+        for (int u = 0; u < 16; ++u)
+          if (q0 + u < P.nsplit) {
+            const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
-              for (int c = 0; c < 4; ++c) x[u][c] = __ldcg(src + c);
+            for (int e = 0; e < 4; ++e) {
+              const float y = __fsub_rn(xs[e], comp[e]);
+              const float t = __fadd_rn(sum[e], y);
+              comp[e] = __fsub_rn(__fsub_rn(t, sum[e]), y);
+              sum[e] = t;
             }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (q0 + u < P.nsplit) {
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const float xs[4] = {x[u][c].x, x[u][c].y, x[u][c].z, x[u][c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int q = 4 * c + e;
-                  const float y = __fsub_rn(xs[e], comp[q]);
-                  const float t = __fadd_rn(sum[q], y);
-                  comp[q] = __fsub_rn(__fsub_rn(t, sum[q]), y);
-                  sum[q] = t;
-                }
-              }
-            }
-        }
-        float pc[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) pc[q] = (float)(coef[kb + q] * ((double)sum[q] - (double)comp[q]));
-        float4 *dpc = reinterpret_cast<float4 *>(P.Pc + (size_t)rr * 32 + kb);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dpc[c] = make_float4(pc[4 * c], pc[4 * c + 1], pc[4 * c + 2], pc[4 * c + 3]);
-        if (P.pc_planes) tc::write_term_planes16(P.pc_planes, (size_t)d_out, (size_t)rr, kb, pc, P.pc_nplanes);
+          }
       }
-      if (tid == 0) P.counters[rb] = 0u;   // ready for the next call
+      float pc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pc[e] = (float)(coef[kb + e] * ((double)sum[e] - (double)comp[e]));
+      *reinterpret_cast<float4 *>(P.Pc + (size_t)rr * 32 + kb) = make_float4(pc[0], pc[1], pc[2], pc[3]);
+      if (P.pc_planes)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          tc::write_term_planes(P.pc_planes, (size_t)d_out, (size_t)rr, kb + e, pc[e], P.pc_nplanes);
     }
   }
 
@@ -434,16 +442,22 @@ cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_
   P.counters = pl.counters;
   const int grid = pl.ncounters * P.nsplit;
   cudaError_t e;
-  if (tc_precision) {
-    const int smem = PLayout<2>::total + 1024;
-    if ((e = ensure_dynamic_smem<k_lr_proj_tc<2>>(smem)) != cudaSuccess) return e;
-    k_lr_proj_tc<2><<<grid, kPThreads, smem, L.stream>>>(P, tmX, tmUT, L.status);
-  } else {
-    const int smem = PLayout<3>::total + 1024;
-    if ((e = ensure_dynamic_smem<k_lr_proj_tc<3>>(smem)) != cudaSuccess) return e;
-    k_lr_proj_tc<3><<<grid, kPThreads, smem, L.stream>>>(P, tmX, tmUT, L.status);
-  }
-  return cudaGetLastError();
+  const int smem = (tc_precision ? PLayout<2>::total : PLayout<3>::total) + 1024;
+  auto kern = tc_precision ? k_lr_proj_tc<2> : k_lr_proj_tc<3>;
+  if (tc_precision) e = ensure_dynamic_smem<k_lr_proj_tc<2>>(smem);
+  else e = ensure_dynamic_smem<k_lr_proj_tc<3>>(smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (P.nsplit > 1) ? 1 : 0;   // the grid barrier needs every CTA resident
+  return cudaLaunchKernelEx(&cfg, kern, P, tmX, tmUT, L.status);
 }
 
 }  // namespace gift

@@ -89,8 +89,6 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   L.sms = ctx->sms;
   L.status = d_status;
   float *planes = (d_in % 32 == 0) ? split : nullptr;
-  if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes) != cudaSuccess)
-    return GIFT_ERR_CUDA;
   LrApply a{};
   a.X = W;
   a.U = f->U;
@@ -108,6 +106,15 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.amax_in = amax_in;
   a.amax_ws = amax_ws;
   a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + 16);
+  if (lr_encode_onepass_ok(L, a, LR_PACK_TENSOR, part, kNoAllocPartFloats)) {
+    if (launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, 2, split) != cudaSuccess) return GIFT_ERR_CUDA;
+    if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
+    if (cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return GIFT_ERR_CUDA;
+    if (launch_lr_encode_onepass(L, LR_PACK_TENSOR, fmt, a, f->mu, part, Pc) != cudaSuccess) return GIFT_ERR_CUDA;
+    return GIFT_OK;
+  }
+  if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes) != cudaSuccess)
+    return GIFT_ERR_CUDA;
   if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
   if (lr_encode_fused_ok(L, a, LR_PACK_TENSOR)) {
     if (cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return GIFT_ERR_CUDA;
