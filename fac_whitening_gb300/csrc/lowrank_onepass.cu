@@ -76,6 +76,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;\n" ::: "memory");
 }
 __device__ __forceinline__ int sw(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+// phase-3 code staging (in the freed W homes): FP8 rows of 32 x 16 bytes, NVFP4 rows of
+// 16 x 16 bytes, 16-byte chunks XOR-swizzled by row; NVFP4 block scales 32 bytes per row after
+constexpr int kOStgScales = 128 * 256;
+__device__ __forceinline__ int stg8(int r, int c) { return r * 512 + ((c ^ (r & 31)) << 4); }
+__device__ __forceinline__ int stg4(int r, int c) { return r * 256 + ((c ^ (r & 15)) << 4); }
 
 // Grid-wide barrier on a monotonic counter (one thread per CTA); false on timeout.
 __device__ __forceinline__ bool grid_barrier(unsigned int *counter, unsigned int target) {
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
       float v[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[e]);
-      const bool in = row < d_out && (c0 + 32 * half) < d_in;
+      // codes are staged in shared memory (the W homes are free now) for coalesced row stores
       if (EPI == LR_PACK_TENSOR) {
         uint32_t w4[8];
 #pragma unroll
@@ -526,11 +531,9 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
           w4[h] = pack4_fp8<F>(__fmul_rn(x[0], sp.m), __fmul_rn(x[1], sp.m), __fmul_rn(x[2], sp.m),
                                __fmul_rn(x[3], sp.m));
         }
-        if (in) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (size_t)row * d_in + c0 + 32 * half);
-          dst[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          dst[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
-        }
+        const int c = 4 * i + 2 * half;   // 16-byte chunk of the CTA's 512-byte code row
+        *reinterpret_cast<uint4 *>(sm + stg8(lr, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        *reinterpret_cast<uint4 *>(sm + stg8(lr, c + 1)) = make_uint4(w4[4], w4[5], w4[6], w4[7]);
       } else {
         uint16_t sc = 0;
         uint32_t cw[4];
@@ -547,12 +550,30 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
           cw[2 * g + 1] = pack8_e2m1(y + 8);
           sc |= (uint16_t)grp.e_code << (8 * g);
         }
-        if (in) {
-          *reinterpret_cast<uint4 *>(a.codes + (((size_t)row * d_in + c0 + 32 * half) >> 1)) =
-              make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          *reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(a.scales) + (size_t)row * (d_in / kNvGroup) +
-                                        (c0 + 32 * half) / kNvGroup) = sc;
-        }
+        *reinterpret_cast<uint4 *>(sm + stg4(lr, 2 * i + half)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint16_t *>(sm + kOStgScales + lr * 32 + 4 * i + 2 * half) = sc;
+      }
+    }
+    // coalesced copy-out of the CTA's code rows (and NVFP4 block scales)
+    tc::named_bar_sync(1, 32 * kOWarps);
+    const int cbase = cb0 * kON;
+    if (EPI == LR_PACK_TENSOR) {
+      for (int r = warp; r < kOM; r += kOWarps) {
+        const int gr = r0 + r, col = cbase + 16 * lane;
+        if (gr < d_out && lane < 4 * nt && col < d_in)
+          *reinterpret_cast<uint4 *>(a.codes + (size_t)gr * d_in + col) = *reinterpret_cast<const uint4 *>(sm + stg8(r, lane));
+      }
+    } else {
+      for (int item = tid; item < kOM * 16; item += 32 * kOWarps) {
+        const int r = item >> 4, c = item & 15, gr = r0 + r, col = cbase + 32 * c;
+        if (gr < d_out && c < 2 * nt && col < d_in)
+          *reinterpret_cast<uint4 *>(a.codes + (((size_t)gr * d_in + col) >> 1)) = *reinterpret_cast<const uint4 *>(sm + stg4(r, c));
+      }
+      for (int item = tid; item < kOM * 16; item += 32 * kOWarps) {
+        const int r = item >> 4, q = item & 15, gr = r0 + r, col = cbase + 32 * q;   // two scale bytes per 32 columns
+        if (gr < d_out && q < 2 * nt && col < d_in)
+          *reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(a.scales) + (size_t)gr * (d_in / kNvGroup) + col / kNvGroup) =
+              *reinterpret_cast<const uint16_t *>(sm + kOStgScales + r * 32 + 2 * q);
       }
     }
   }
