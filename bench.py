@@ -277,15 +277,42 @@ def main_gift(args):
     for i, L in enumerate(gl):   # warm-up refresh of the first layer
         f = G.Factor.empty("lowrank", d_out, d_in, 32, device=dev)
         factors.append(f)
+    # the codec uses the FP32-precision factors; the tensor-core (TC precision) refresh is
+    # timed beside it on the same activations
+    refresh = {}
+    for prec in ("tc", "fp32"):
+        if not gl:
+            break
+        scratch = [G.Factor.empty("lowrank", d_out, d_in, 32, device=dev) for _ in gl] if prec == "tc" else factors
+        G.gift_factor_update(ctx, scratch[0], gl[0]["a"], seed=1, prec=prec, ws=fws, status=st)   # warm-up
+        torch.cuda.synchronize()
+        fe0.record()
+        for i, L in enumerate(gl):
+            G.gift_factor_update(ctx, scratch[i], L["a"], seed=1000 + i, prec=prec, ws=fws, status=st)
+        fe1.record()
+        torch.cuda.synchronize()
+        refresh[prec] = fe0.elapsed_time(fe1) / len(gl)
+    factor_ms = refresh.get("fp32", 0.0)
+    # the K-FAC factor alone on the tensor cores (gift_kfac_factor: transpose, tcgen05 SYRK of
+    # the lower tiles, mirror), d (d + 1) T flops
+    kfac = None
     if gl:
-        G.gift_factor_update(ctx, factors[0], gl[0]["a"], seed=1, ws=fws, status=st)
-    torch.cuda.synchronize()
-    fe0.record()
-    for i, L in enumerate(gl):
-        G.gift_factor_update(ctx, factors[i], L["a"], seed=1000 + i, ws=fws, status=st)
-    fe1.record()
-    torch.cuda.synchronize()
-    factor_ms = fe0.elapsed_time(fe1) / max(len(gl), 1)
+        Abuf = torch.empty(d_in, d_in, device=dev)
+        kws = torch.zeros(G.gift_workspace_bytes(ctx, "kfac_factor", "identity", FMT, "tensor", d_in, d_in, T),
+                          dtype=torch.uint8, device=dev)
+        G.gift_kfac_factor(ctx, gl[0]["a"], Abuf, prec="tc", ws=kws, status=st)
+        torch.cuda.synchronize()
+        fe0.record()
+        for _ in range(5):
+            G.gift_kfac_factor(ctx, gl[0]["a"], Abuf, prec="tc", ws=kws, status=st)
+        fe1.record()
+        torch.cuda.synchronize()
+        kms = fe0.elapsed_time(fe1) / 5
+        kflops = float(d_in) * (d_in + 1) * T
+        kfac = {"ms": kms, "tflops": kflops / (kms * 1e-3) / 1e12, "peak_tflops": bf16_peak,
+                "frac": kflops / (kms * 1e-3) / 1e12 / bf16_peak, "peak_kind": peak_kind + " bf16 burst",
+                "flops": kflops, "shape": f"a {T}x{d_in} BF16 -> A {d_in}x{d_in} FP32"}
+        del Abuf, kws
     syrk_flops = float(d_in) * d_in * T        # a^T a over T tokens (both triangles counted once)
     for L in gl:
         del L["a"]
@@ -496,9 +523,12 @@ def main_gift(args):
                            "parallelism": f"replicas x{world}", "streams_per_stage": nstr},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": kernels_per_step * args.steps, "stages": stages,
-                "factor_refresh": {"ms_per_layer": factor_ms, "syrk_tflops": syrk_flops / (factor_ms * 1e-3) / 1e12,
-                                   "note": "whole refresh (SYRK + rank-32 subspace iteration + Jacobi) per layer; "
-                                           "TFLOP/s counts the a^T a flops only"},
+                "factor_syrk": kfac,
+                "factor_refresh": {p: {"ms_per_layer": ms_, "syrk_tflops": syrk_flops / (ms_ * 1e-3) / 1e12}
+                                   for p, ms_ in refresh.items()} | {
+                                   "note": "whole refresh (SYRK + rank-32 subspace iteration + Jacobi) per layer, "
+                                           "BF16 activations; TFLOP/s counts the a^T a flops only; tc = A on "
+                                           "tcgen05 (TC precision), fp32 = FP32 SIMT (the factors the codec uses)"},
                 "device_status": status_word}
         print(json.dumps(line), flush=True)
     if world > 1:

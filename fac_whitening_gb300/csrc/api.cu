@@ -78,13 +78,18 @@ struct FactorWs {
   double *A64 = nullptr, *Ai64 = nullptr, *work = nullptr;
   float *Gf = nullptr;
   double *G64 = nullptr, *Gi64 = nullptr;
+  void *at = nullptr;       // BF16 transpose of the activations (tensor-core SYRK)
   size_t bytes = 0;
 };
 
-FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in) {
+FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in, int T) {
   FactorWs w;
   Carve c(base);
   w.A = c.take<float>((size_t)d_in * d_in);
+  if (T > 0) {
+    const int dmax = (kind == GIFT_XF_CHOL_TWO_SIDED && d_out > d_in) ? d_out : d_in;
+    w.at = c.take<uint8_t>(syrk_tc_scratch_bytes(dmax, T));
+  }
   if (kind == GIFT_XF_LOWRANK) {
     w.k = d_in < 64 ? d_in : 64;
     w.gsplits = d_in / 256;
@@ -276,13 +281,13 @@ int gift_version(void) { return GIFT_VERSION_MAJOR * 1000 + GIFT_VERSION_MINOR; 
 
 size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gift_format fmt,
                             gift_scaling scaling, int d_out, int d_in, int T, int rank) {
-  (void)T;
   (void)rank;
   if (!ctx || d_out <= 0 || d_in <= 0 || !valid_kind(kind) || !valid_fmt(fmt) || !valid_scaling(scaling))
     return (size_t)-1;
+  if (op == GIFT_OP_KFAC_FACTOR) return T > 0 ? syrk_tc_scratch_bytes(d_in, T) : (size_t)-1;
   if (op == GIFT_OP_FACTOR_UPDATE) {
     if (kind == GIFT_XF_IDENTITY) return 0;
-    return factor_layout(nullptr, ctx->sms, kind, d_out, d_in).bytes;
+    return factor_layout(nullptr, ctx->sms, kind, d_out, d_in, T).bytes;
   }
   if (op != GIFT_OP_ENCODE && op != GIFT_OP_DECODE && op != GIFT_OP_AMAX) return (size_t)-1;
   return codec_layout(nullptr, ctx->sms, op, kind, d_out, d_in).bytes;
@@ -313,11 +318,45 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
 }
 
 // -----------------------------------------------------------------------------------------
+namespace {
+
+// A = x^T x / T (full symmetric, FP32): tensor cores for TC precision and BF16 input where the
+// shape allows (at = scratch of syrk_tc_scratch_bytes(d, T) bytes), FP32 SIMT otherwise.
+cudaError_t kfac_syrk(const Launch &L, const void *x, bool bf16, int T, int d, gift_precision prec, void *at,
+                      float *out) {
+  if (prec == GIFT_PREC_TC && bf16 && at && syrk_tc_ok(d, T, x, at, out)) {
+    cudaError_t e = launch_syrk_tc(L, x, T, d, 1.0f / (float)T, at, out);
+    if (e != cudaSuccess) return e;
+    return launch_mirror_lower(L, out, d);
+  }
+  GemmArgs g{};
+  g.A = x; g.B = x; g.C = out;
+  g.M = d; g.N = d; g.K = T; g.lda = d; g.ldb = d; g.ldc = d;
+  g.transA = true; g.transB = false; g.a_bf16 = bf16; g.b_bf16 = bf16;
+  g.lower_tiles = true; g.alpha = 1.0f / (float)T;
+  cudaError_t e = launch_sgemm(L, g);
+  if (e != cudaSuccess) return e;
+  return launch_mirror_lower(L, out, d);
+}
+
+}  // namespace
+
+gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int T, int d, gift_precision prec,
+                             float *A_out, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  if (!ctx || !a || !A_out || T < 1 || d < 1) return GIFT_ERR_INVALID_ARG;
+  if (a_dt != GIFT_DT_F32 && a_dt != GIFT_DT_BF16) return GIFT_ERR_INVALID_ARG;
+  if (prec != GIFT_PREC_FP32 && prec != GIFT_PREC_TC) return GIFT_ERR_INVALID_ARG;
+  if (prec == GIFT_PREC_TC && (!ws || ws_bytes < syrk_tc_scratch_bytes(d, T))) return GIFT_ERR_INVALID_ARG;
+  const Launch L = mk(ctx, d_status, stream);
+  CK(kfac_syrk(L, a, a_dt == GIFT_DT_BF16, T, d, prec, prec == GIFT_PREC_TC ? ws : nullptr, A_out));
+  return GIFT_OK;
+}
+
 gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
                                const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
                                void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
-  (void)prec;
   if (!ctx || !f || !a || T < 1) return GIFT_ERR_INVALID_ARG;
+  if (prec != GIFT_PREC_FP32 && prec != GIFT_PREC_TC) return GIFT_ERR_INVALID_ARG;
   const int d_in = f->d_in, d_out = f->d_out;
   if (d_in <= 0 || d_out <= 0) return GIFT_ERR_INVALID_ARG;
   if (a_dt != GIFT_DT_F32 && a_dt != GIFT_DT_BF16) return GIFT_ERR_INVALID_ARG;
@@ -326,21 +365,14 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
   if (cs != GIFT_OK) return cs;
   if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!delta || (d_dt != GIFT_DT_F32 && d_dt != GIFT_DT_BF16)))
     return GIFT_ERR_INVALID_ARG;
-  const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in);
+  const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in, T);
   if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
-  const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in);
+  const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in, T);
   const Launch L = mk(ctx, d_status, stream);
 
   // A = a^T a / T (lower tiles, then mirrored)
   auto syrk = [&](const void *x, bool bf16, int d, float *out) -> cudaError_t {
-    GemmArgs g{};
-    g.A = x; g.B = x; g.C = out;
-    g.M = d; g.N = d; g.K = T; g.lda = d; g.ldb = d; g.ldc = d;
-    g.transA = true; g.transB = false; g.a_bf16 = bf16; g.b_bf16 = bf16;
-    g.lower_tiles = true; g.alpha = 1.0f / (float)T;
-    cudaError_t e = launch_sgemm(L, g);
-    if (e != cudaSuccess) return e;
-    return launch_mirror_lower(L, out, d);
+    return kfac_syrk(L, x, bf16, T, d, prec, w.at, out);
   };
   CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
 

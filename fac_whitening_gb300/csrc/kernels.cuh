@@ -115,6 +115,12 @@ cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_
                               const float *sigma, int rank, bool inverse, bool tc_precision, float *part, float *Pc,
                               float *split);
 
+// syrk_tc.cu: A = scale * x^T x for BF16 x (T x d) on tcgen05 (lower tiles; mirror after).
+// `at` is scratch of syrk_tc_scratch_bytes(d, T) bytes (the transpose of x).
+bool syrk_tc_ok(int d, int T, const void *a, const void *at, const float *out);
+size_t syrk_tc_scratch_bytes(int d, int T);
+cudaError_t launch_syrk_tc(const Launch &L, const void *a, int T, int d, float scale, void *at, float *out);
+
 // Sets a kernel's opt-in dynamic shared-memory size once per device and kernel (so no
 // attribute call happens inside a stream capture after the first eager call).  Keyed on the
 // kernel itself: instantiations that share a function type keep separate flags.

@@ -25,7 +25,7 @@ SCALING = {"tensor": 0, "block128": 1}
 XFORM = {"identity": 0, "lowrank": 1, "chol_input": 2, "chol_two_sided": 3}
 PREC = {"fp32": 0, "tc": 1}
 DTYPE = {"f32": 0, "bf16": 1}
-OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3}
+OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3, "kfac_factor": 4}
 OPT_SUBSPACE_ITERS = 0
 
 _vp = ctypes.c_void_p
@@ -63,6 +63,7 @@ def _declare(lib):
         "gift_code_sizes": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
         "gift_factor_update": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _vp, _i, ctypes.c_uint64, _i,
                                     _vp, _sz, _vp, _vp]),
+        "gift_kfac_factor": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
         "gift_amax": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]),
         "gift_encode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                              _vp, _vp, _sz, _vp, _vp]),
@@ -219,6 +220,15 @@ def gift_factor_update(ctx: Context, f: Factor, a, delta=None, seed: int = 0, pr
     _check(lib().gift_factor_update(ctx.handle, ctypes.byref(st), _p(a), a_dt, a.shape[0], _p(delta), d_dt,
                                     seed, PREC[prec], _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                     _p(status), _stream(stream)), "gift_factor_update")
+
+
+def gift_kfac_factor(ctx: Context, a, A_out, prec: str = "fp32", ws=None, status=None, stream=None):
+    import torch
+    a_dt = DTYPE["bf16"] if a.dtype == torch.bfloat16 else DTYPE["f32"]
+    T, d = a.shape
+    _check(lib().gift_kfac_factor(ctx.handle, _p(a), a_dt, T, d, PREC[prec], _p(A_out), _p(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(), _p(status), _stream(stream)),
+           "gift_kfac_factor")
 
 
 def gift_amax(ctx: Context, f: Optional[Factor], W, fmt: str, scaling: str, amax_accum, residual=None,

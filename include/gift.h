@@ -132,7 +132,8 @@ typedef enum {
   GIFT_OP_FACTOR_UPDATE = 0,
   GIFT_OP_ENCODE = 1,
   GIFT_OP_DECODE = 2,
-  GIFT_OP_AMAX = 3
+  GIFT_OP_AMAX = 3,
+  GIFT_OP_KFAC_FACTOR = 4
 } gift_op;
 
 /* Tunables for gift_set_option. */
@@ -153,7 +154,8 @@ const char *gift_last_error(void);
 
 /* Bytes of caller-provided device workspace an operation needs (0 if none).
  * Host-only; returns (size_t)-1 for invalid arguments.  T is used by
- * GIFT_OP_FACTOR_UPDATE only, rank by the LOWRANK kind only. */
+ * GIFT_OP_FACTOR_UPDATE and GIFT_OP_KFAC_FACTOR only (the latter also reads d_in = d and
+ * ignores kind, format and scaling), rank by the LOWRANK kind only. */
 size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gift_format fmt,
                             gift_scaling scaling, int d_out, int d_in, int T, int rank);
 
@@ -176,11 +178,30 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
  *           NOT_CONVERGED when the Jacobi sweeps do not converge.
  *  CHOL_* : A (and G) are formed in FP32 and factored in FP64; L and L^-1 are stored in
  *           FP32.  d_status: NOT_PD on a non-positive pivot.
- *  ws     : device workspace of gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ...) bytes.
+ *  prec   : GIFT_PREC_FP32 forms A (and G) with FP32 SIMT accumulation.  GIFT_PREC_TC with
+ *           BF16 activations (d a multiple of 256, T of 64) forms them on the tensor cores:
+ *           exact BF16 products, tensor-core FP32 accumulation over T (not round to
+ *           nearest); other cases fall back to the FP32 path.
+ *  ws     : device workspace of gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ..., T, ...)
+ *           bytes; it includes a BF16 transpose of the activations (max d x T x 2 bytes).
  * Returns INVALID_ARG on null pointers, T < 1, rank outside [1, min(32, d_in)]. */
 gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
                                const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
                                void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* The K-FAC factor alone ([notes] prerequisites, eq. (4): A = a^T a / T), the first step of
+ * gift_factor_update, for callers that combine factors before factoring them (for example
+ * averaging A over the data-parallel replicas or across refreshes).
+ *  a     : device, T x d activations of type a_dt, row-major.
+ *  prec  : as in gift_factor_update: GIFT_PREC_TC with BF16 activations (d a multiple of
+ *          256, T of 64) on the tensor cores, otherwise FP32 SIMT.
+ *  A_out : device, d x d FP32, row-major; receives the full symmetric matrix.
+ *  ws    : device workspace of gift_workspace_bytes(GIFT_OP_KFAC_FACTOR, ..., d_out, d_in = d,
+ *          T, ...) bytes (the BF16 transpose of the activations); may be NULL with
+ *          GIFT_PREC_FP32.
+ * Returns INVALID_ARG on null pointers, d < 1, T < 1, or a workspace too small for TC. */
+gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int T, int d, gift_precision prec,
+                             float *A_out, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
 
 /* Amax of the tensor that gift_encode would quantise (the transformed gradient, plus the
  * residual when one is given), max-accumulated into amax_accum: the AllReduceMax of the

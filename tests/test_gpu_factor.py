@@ -14,7 +14,7 @@ from gpu_util import DEV, ctx, rel_fro, status, t
 pytestmark = pytest.mark.gpu
 
 
-def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None):
+def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None, prec="fp32"):
     d_in = a.shape[1]
     f = G.Factor.empty(kind, d_out, d_in, rank)
     n = G.gift_workspace_bytes(ctx(), "factor_update", kind, "e4m3", "tensor", d_out, d_in, a.shape[0], rank)
@@ -22,14 +22,14 @@ def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None):
     st = status()
     if iters:
         G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, iters)
-    G.gift_factor_update(ctx(), f, a, delta=delta, seed=seed, ws=w, status=st)
+    G.gift_factor_update(ctx(), f, a, delta=delta, seed=seed, prec=prec, ws=w, status=st)
     torch.cuda.synchronize()
     if iters:
         G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, 10)
     return f, w, int(st.item())
 
 
-def check_lowrank(f, a64, rank, st):
+def check_lowrank(f, a64, rank, st, sigma_rtol=1e-3):
     assert st == 0
     A = O.kfac_factor(a64)
     ev = np.sort(np.linalg.eigvalsh(A))[::-1]
@@ -39,7 +39,7 @@ def check_lowrank(f, a64, rank, st):
     d = A.shape[0]
     sigma = float(f.sigma.item())
     want_sigma = 1.0 if rank == d else (np.trace(A) - ev[:rank].sum()) / (d - rank)
-    assert abs(sigma - want_sigma) <= 1e-3 * abs(want_sigma)
+    assert abs(sigma - want_sigma) <= sigma_rtol * abs(want_sigma)
     np.testing.assert_allclose(U.T @ U, np.eye(rank), atol=1e-5)
     # residual bound: some exact eigenvalue lies within ||A u - mu u|| of mu
     res = np.linalg.norm(A @ U - U * mu, axis=0)
@@ -64,6 +64,52 @@ def test_factor_lowrank_bf16_steep():
     _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
     f, _, st = run_factor("lowrank", a, 128)
     check_lowrank(f, a.double().cpu().numpy(), 32, st)
+
+
+def test_factor_tc_syrk_exact_on_integer_activations():
+    # tensor-core SYRK (TC precision, BF16 activations, d % 256 == 0, T % 64 == 0): with small
+    # integer activations every partial sum is an exactly representable FP32 integer, so the
+    # result must equal a^T a / T exactly (T a power of two), tiles, transpose and mirror included
+    rng = np.random.default_rng(11)
+    T, d = 1024, 512
+    a = rng.integers(-2, 3, size=(T, d)).astype(np.float32)
+    at = torch.tensor(a, dtype=torch.bfloat16, device=DEV)
+    f, w, st = run_factor("lowrank", at, 256, prec="tc")
+    assert st == 0
+    A_gpu = w[: d * d * 4].view(torch.float32).view(d, d).cpu().double().numpy()
+    np.testing.assert_array_equal(A_gpu, (a.astype(np.float64).T @ a.astype(np.float64)) / T)
+
+
+def test_factor_lowrank_bf16_steep_tc():
+    # same inputs as the FP32 test, A on the tensor cores: eigenvalues within 1e-3, and A
+    # itself within the accumulation error of 256 tensor-core K steps.  sigma = (tr A -
+    # sum mu) / (d - r) cancels on this steep spectrum (sigma / mu_1 ~ 1e-5), which amplifies
+    # the accumulation error; its bound follows from the TC transform tolerance: alpha =
+    # sigma^-1/2 moves by half of sigma's relative error, 1e-2 -> 5e-3 < 2e-2
+    spec = synth.LayerSpec("m", 128, 1024, T=4096, exponent=1.2, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
+    f, w, st = run_factor("lowrank", a, 128, prec="tc")
+    a64 = a.double().cpu().numpy()
+    check_lowrank(f, a64, 32, st, sigma_rtol=1e-2)
+    A_gpu = w[: 1024 * 1024 * 4].view(torch.float32).view(1024, 1024).cpu().double().numpy()
+    assert rel_fro(A_gpu, O.kfac_factor(a64)) <= 1e-4
+
+
+@pytest.mark.parametrize("prec", ["fp32", "tc"])
+def test_kfac_factor_entry_point(prec):
+    # A = a^T a / T alone, both precisions; integer activations make every sum exact
+    rng = np.random.default_rng(13)
+    T, d = 512, 256
+    a = rng.integers(-3, 4, size=(T, d)).astype(np.float32)
+    at = torch.tensor(a, dtype=torch.bfloat16, device=DEV)
+    A = torch.empty(d, d, device=DEV)
+    n = G.gift_workspace_bytes(ctx(), "kfac_factor", "identity", "e4m3", "tensor", d, d, T)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    st = status()
+    G.gift_kfac_factor(ctx(), at, A, prec=prec, ws=w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(A.cpu().double().numpy(), a.astype(np.float64).T @ a.astype(np.float64) / T)
 
 
 def test_factor_exact_rank_equals_d_in():
