@@ -92,9 +92,9 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
   }
   if (kind == GIFT_XF_LOWRANK) {
     w.k = d_in < 64 ? d_in : 64;
-    w.gsplits = d_in / 256;
+    w.gsplits = d_in / 64;   // the FP64 Gram slices: up to one CTA per SM
     if (w.gsplits < 1) w.gsplits = 1;
-    if (w.gsplits > 64) w.gsplits = 64;
+    if (w.gsplits > sms) w.gsplits = sms;
     const int rowtiles = (d_in + 127) / 128;
     w.ysplits = (2 * sms + rowtiles - 1) / rowtiles;
     const int maxs = (d_in + 255) / 256;

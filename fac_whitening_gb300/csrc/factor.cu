@@ -172,6 +172,10 @@ __global__ void __launch_bounds__(256) k_small_chol_rinv(const double *__restric
     }
     __syncthreads();
   }
+  // reciprocals of the pivots once (FP64 division is slow), kept in the unused upper triangle's
+  // diagonal-adjacent column k of S (S has 65 columns)
+  for (int i = tid; i < k; i += 256) S[i][64] = 1.0 / S[i][i];
+  __syncthreads();
   for (int c = tid; c < k; c += 256) {
     for (int i = 0; i < k; ++i) {
       if (i < c) {
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(256) k_small_chol_rinv(const double *__restric
       }
       double s = (i == c) ? 1.0 : 0.0;
       for (int q = c; q < i; ++q) s = fma(-S[i][q], X[q][c], s);
-      X[i][c] = s / S[i][i];
+      X[i][c] = s * S[i][64];
     }
   }
   __syncthreads();
