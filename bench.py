@@ -274,8 +274,8 @@ def main_gift(args):
                       dtype=torch.uint8, device=dev)
     factors = []
     fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i, L in enumerate(gl):   # warm-up refresh of the first layer
-        f = G.Factor.empty("lowrank", d_out, d_in, 32, device=dev)
+    for i, L in enumerate(gl):   # the codec's factors carry their U term planes (refreshed with U)
+        f = G.Factor.empty("lowrank", d_out, d_in, 32, device=dev, planes=True)
         factors.append(f)
     # the codec uses the FP32-precision factors; the tensor-core (TC precision) refresh is
     # timed beside it on the same activations

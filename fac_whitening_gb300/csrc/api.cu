@@ -151,6 +151,7 @@ gift_status check_factor(const gift_factor *f, int d_out, int d_in) {
   if (f->kind == GIFT_XF_LOWRANK) {
     if (!f->U || !f->mu || !f->sigma) return GIFT_ERR_INVALID_ARG;
     if (f->rank < 1 || f->rank > kMaxRank || f->rank > d_in) return GIFT_ERR_INVALID_ARG;
+    if (f->planes && !aligned16(f->planes)) return GIFT_ERR_INVALID_ARG;
   } else {
     if (!f->LA || !f->LAinv) return GIFT_ERR_INVALID_ARG;
     if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!f->LG || !f->LGinv)) return GIFT_ERR_INVALID_ARG;
@@ -212,6 +213,7 @@ LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const
   a.d_in = d_in;
   a.inverse = inverse;
   a.split = (d_in % 32 == 0) ? w.split : nullptr;
+  if (a.split) lr_u_planes(f->planes, w.split, d_out, d_in, &a.u_planes, &a.ut_planes);
   return a;
 }
 
@@ -220,7 +222,7 @@ LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const
 cudaError_t lr_prepare(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w,
                        bool inverse, gift_precision prec) {
   return lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, X, d_out, d_in, inverse, prec == GIFT_PREC_TC, w.part,
-                        w.Pc, (d_in % 32 == 0) ? w.split : nullptr);
+                        w.Pc, (d_in % 32 == 0) ? w.split : nullptr, f->planes);
 }
 
 }  // namespace
@@ -341,6 +343,17 @@ cudaError_t kfac_syrk(const Launch &L, const void *x, bool bf16, int T, int d, g
 
 }  // namespace
 
+size_t gift_factor_planes_bytes(int d_in) { return d_in > 0 ? lr_factor_planes_bytes(d_in) : (size_t)-1; }
+
+gift_status gift_factor_prepare(gift_ctx *ctx, const gift_factor *f, cudaStream_t stream) {
+  if (!ctx || !f || f->kind != GIFT_XF_LOWRANK || !f->U || !f->planes) return GIFT_ERR_INVALID_ARG;
+  if (f->d_in <= 0 || f->rank < 1 || f->rank > kMaxRank || f->rank > f->d_in || !aligned16(f->planes))
+    return GIFT_ERR_INVALID_ARG;
+  const Launch L = mk(ctx, nullptr, stream);
+  CK(launch_lr_factor_planes(L, f->U, f->d_in, f->rank, f->planes));
+  return GIFT_OK;
+}
+
 gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int T, int d, gift_precision prec,
                              float *A_out, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
   if (!ctx || !a || !A_out || T < 1 || d < 1) return GIFT_ERR_INVALID_ARG;
@@ -425,6 +438,7 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
     }
     CK(launch_jacobi(L, w.G, k, w.ev, w.V));
     CK(launch_lowrank_outputs(L, w.Q, d_in, k, w.V, w.ev, w.tr, f->rank, f->U, f->mu, f->sigma));
+    if (f->planes) CK(launch_lr_factor_planes(L, f->U, d_in, f->rank, f->planes));
     return GIFT_OK;
   }
 
@@ -519,7 +533,7 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
       o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + 16);
       const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
       if (lr_encode_onepass_ok(L, o, epi, w.part, lr_part_floats(ctx->sms, d_out, d_in))) {
-        CK(launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split));
+        if (!f->planes) CK(launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split));
         if (!amax_in) CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
         CK(cudaMemsetAsync(o.grid_counter, 0, sizeof(unsigned int), stream));
         CK(launch_lr_encode_onepass(L, epi, fmt, o, f->mu, w.part, w.Pc));

@@ -55,7 +55,7 @@ cudaError_t launch_lr_finalize(const Launch &L, const float *part, int nsplit, i
 // otherwise the FP32-SIMT projection and finalize).  `part` holds lr_part_floats floats.
 cudaError_t lr_prepare_all(const Launch &L, const float *U, const float *mu, const float *sigma, int rank,
                            const float *X, int d_out, int d_in, bool inverse, bool tc_precision, float *part,
-                           float *Pc, float *split);
+                           float *Pc, float *split, const void *cached_planes = nullptr);
 size_t lr_part_floats(int sms, int d_out, int d_in);
 // Fused apply V = alpha X + Pc U^T (+ R), alpha = sigma^-1/2 (or sigma^1/2 for the map back).
 enum LrEpi { LR_AMAX = 0, LR_PACK_TENSOR = 1, LR_BLOCK = 2, LR_NVFP4 = 3, LR_STORE = 4, LR_BLOCK_AMAX = 5 };
@@ -79,6 +79,8 @@ struct LrApply {
                             // otherwise FP32 precision (three BF16 terms, six products)
   float *split;             // BF16 term planes (tc.cuh): Pc planes (2 x d_out x 32 floats), then U
   unsigned int *grid_counter;   // fused encode: grid-barrier word, zero before the launch
+  const uint16_t *u_planes;     // U term planes for the apply (2 x d_in rows of 64 BF16)
+  const uint16_t *ut_planes;    // U^T term planes for the projection (3 x 32 rows of d_in BF16)
 };
 cudaError_t launch_lr_apply(const Launch &L, int epi, int fmt, const LrApply &a);
 // lowrank_tc.cu: the same apply on tcgen05 tensor cores (vectorised shapes only)
@@ -106,6 +108,12 @@ struct LrPlanes {
   int ncounters;
 };
 LrPlanes lr_planes(float *split, int d_out, int d_in);
+// U planes of a factor: its cached planes (gift_factor.planes, laid out [u | ut]) when given,
+// otherwise the workspace's.
+void lr_u_planes(const void *cached, float *split, int d_out, int d_in, const uint16_t **u, const uint16_t **ut);
+size_t lr_factor_planes_bytes(int d_in);
+// Write the U planes of (U, rank) into a factor's cached planes.
+cudaError_t launch_lr_factor_planes(const Launch &L, const float *U, int d_in, int rank, void *planes);
 int lr_proj_tc_splits(int sms, int d_out, int d_in);
 bool lr_proj_tc_ok(const float *X, int d_in, const float *split);
 // U planes in both layouts (and the counters zeroed); then P, Pc and the Pc planes.
@@ -113,7 +121,7 @@ cudaError_t launch_lr_split_u_all(const Launch &L, const float *U, int d_out, in
                                   float *split);
 cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_in, const float *mu,
                               const float *sigma, int rank, bool inverse, bool tc_precision, float *part, float *Pc,
-                              float *split);
+                              float *split, const uint16_t *ut_planes);
 
 // syrk_tc.cu: A = scale * x^T x for BF16 x (T x d) on tcgen05 (lower tiles; mirror after).
 // `at` is scratch of syrk_tc_scratch_bytes(d, T) bytes (the transpose of x).

@@ -457,11 +457,18 @@ cudaError_t launch_lr_proj(const Launch &L, const float *X, int d_out, int d_in,
 
 cudaError_t lr_prepare_all(const Launch &L, const float *U, const float *mu, const float *sigma, int rank,
                            const float *X, int d_out, int d_in, bool inverse, bool tc_precision, float *part,
-                           float *Pc, float *split) {
+                           float *Pc, float *split, const void *cached_planes) {
   cudaError_t e;
   if (split && lr_proj_tc_ok(X, d_in, split)) {
-    if ((e = launch_lr_split_u_all(L, U, d_out, d_in, rank, tc_precision ? 1 : 2, split)) != cudaSuccess) return e;
-    return launch_lr_proj_tc(L, X, d_out, d_in, mu, sigma, rank, inverse, tc_precision, part, Pc, split);
+    const uint16_t *u = nullptr, *ut = nullptr;
+    lr_u_planes(cached_planes, split, d_out, d_in, &u, &ut);
+    if (!cached_planes) {
+      if ((e = launch_lr_split_u_all(L, U, d_out, d_in, rank, tc_precision ? 1 : 2, split)) != cudaSuccess) return e;
+    } else {
+      const LrPlanes pl = lr_planes(split, d_out, d_in);   // the projection's barrier word
+      if ((e = cudaMemsetAsync(pl.counters, 0, sizeof(unsigned int), L.stream)) != cudaSuccess) return e;
+    }
+    return launch_lr_proj_tc(L, X, d_out, d_in, mu, sigma, rank, inverse, tc_precision, part, Pc, split, ut);
   }
   const int nsplit = lr_proj_splits(L.sms, d_out, d_in);
   if ((e = launch_lr_proj(L, X, d_out, d_in, U, rank, part, nsplit)) != cudaSuccess) return e;
@@ -469,7 +476,7 @@ cudaError_t lr_prepare_all(const Launch &L, const float *U, const float *mu, con
   const int terms = tc_precision ? 1 : 3;
   if ((e = launch_lr_finalize(L, part, nsplit, d_out, mu, sigma, rank, inverse, Pc, pc_terms, terms)) != cudaSuccess)
     return e;
-  if (!pc_terms) return cudaSuccess;
+  if (!pc_terms || cached_planes) return cudaSuccess;
   LrApply a{};
   a.U = U;
   a.rank = rank;

@@ -636,8 +636,8 @@ cudaError_t onepass_launch(const Launch &L, const OnePassParams &P, int grid) {
   constexpr int NPL = NT - 1;
   CUtensorMap tmW, tmUT, tmU, tmPc;
   if (!omap(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.X, (uint64_t)a.d_out, (uint64_t)a.d_in, 32, kOM) ||
-      !omap(&tmUT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pl.ut, 96, (uint64_t)a.d_in, kON, 32) ||
-      !omap(&tmU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pl.u, (uint64_t)NPL * a.d_in, 32, 32, kON) ||
+      !omap(&tmUT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ut_planes, 96, (uint64_t)a.d_in, kON, 32) ||
+      !omap(&tmU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.u_planes, (uint64_t)NPL * a.d_in, 32, 32, kON) ||
       !omap(&tmPc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pl.pc, (uint64_t)NPL * a.d_out, 32, 32, kOM))
     return cudaErrorInvalidValue;
   const int smem = kOSmemTotal + 1024;

@@ -406,6 +406,25 @@ LrPlanes lr_planes(float *split, int d_out, int d_in) {
   return p;
 }
 
+void lr_u_planes(const void *cached, float *split, int d_out, int d_in, const uint16_t **u, const uint16_t **ut) {
+  if (cached) {
+    *u = static_cast<const uint16_t *>(cached);
+    *ut = *u + (size_t)128 * d_in;
+  } else {
+    const LrPlanes pl = lr_planes(split, d_out, d_in);
+    *u = pl.u;
+    *ut = pl.ut;
+  }
+}
+
+size_t lr_factor_planes_bytes(int d_in) { return (size_t)448 * d_in; }
+
+cudaError_t launch_lr_factor_planes(const Launch &L, const float *U, int d_in, int rank, void *planes) {
+  uint16_t *u = static_cast<uint16_t *>(planes);
+  k_split_u<<<(d_in + 31) / 32, 256, 0, L.stream>>>(U, d_in, rank, 2, u, u + (size_t)128 * d_in, nullptr, 0);
+  return cudaGetLastError();
+}
+
 bool lr_proj_tc_ok(const float *X, int d_in, const float *split) {
   return d_in % 32 == 0 && aligned16(X) && aligned16(split) && proj_encoder() != nullptr;
 }
@@ -420,11 +439,11 @@ cudaError_t launch_lr_split_u_all(const Launch &L, const float *U, int d_out, in
 
 cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_in, const float *mu,
                               const float *sigma, int rank, bool inverse, bool tc_precision, float *part, float *Pc,
-                              float *split) {
+                              float *split, const uint16_t *ut_planes) {
   const LrPlanes pl = lr_planes(split, d_out, d_in);
   CUtensorMap tmX, tmUT;
   if (!map2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, X, (uint64_t)d_out, (uint64_t)d_in, 32, kPM) ||
-      !map2d(&tmUT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pl.ut, 96, (uint64_t)d_in, kPK, 32))
+      !map2d(&tmUT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ut_planes, 96, (uint64_t)d_in, kPK, 32))
     return cudaErrorInvalidValue;
   ProjParams P;
   P.mu = mu;

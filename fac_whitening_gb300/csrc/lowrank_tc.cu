@@ -724,8 +724,8 @@ size_t lr_pipe_split_floats(int d_out, int d_in) {
 // in lowrank.cu.
 bool lr_apply_tc_ok(const LrApply &a, int epi) {
   if (epi != LR_AMAX && epi != LR_PACK_TENSOR && epi != LR_NVFP4 && epi != LR_STORE) return false;
-  if (!a.split) return false;
-  bool ok = (a.d_in % 32 == 0) && aligned16(a.X) && aligned16(a.split) && !a.R &&
+  if (!a.split || !a.u_planes) return false;
+  bool ok = (a.d_in % 32 == 0) && aligned16(a.X) && aligned16(a.split) && aligned16(a.u_planes) && !a.R &&
             (!a.tout || aligned16(a.tout)) && a.rank >= 1 && a.rank <= 32;
   if (epi == LR_STORE) ok = ok && aligned16(a.out);
   if (epi == LR_PACK_TENSOR || epi == LR_NVFP4) ok = ok && aligned16(a.codes);
@@ -737,7 +737,7 @@ static int pipe_planes(const LrApply &a) { return a.terms == 1 ? 1 : 2; }
 
 // U planes go after the Pc planes (which the finalize writes) in the workspace.
 cudaError_t launch_lr_split_u(const Launch &L, const LrApply &a) {
-  uint16_t *uplanes = reinterpret_cast<uint16_t *>(a.split + (size_t)2 * 32 * a.d_out);
+  uint16_t *uplanes = reinterpret_cast<uint16_t *>(a.split + (size_t)2 * 32 * a.d_out);   // workspace planes
   const size_t n = (size_t)a.d_in * 32;
   int grid = (int)((n + 255) / 256);
   if (grid > L.sms * 8) grid = L.sms * 8;
@@ -748,7 +748,7 @@ cudaError_t launch_lr_split_u(const Launch &L, const LrApply &a) {
 template <int EPI, int F, int NPL>
 static cudaError_t pipe_launch(const Launch &L, const LrApply &a) {
   CUtensorMap tmW, tmB;
-  const float *ut = a.split + (size_t)2 * 32 * a.d_out;
+  const void *ut = a.u_planes;
   // the U planes are 128-byte rows, mapped as 32 FP32 "columns" (TMA copies bytes)
   if (!make_map(&tmW, a.X, (uint64_t)a.d_out, (uint64_t)a.d_in, kTileM) ||
       !make_map(&tmB, ut, (uint64_t)NPL * a.d_in, 32, kTileN))
@@ -818,7 +818,7 @@ template <int EPI, int F, int NPL, bool TOUT>
 static cudaError_t fused_launch(const Launch &L, const LrApply &a, int grid, int cpr) {
   CUtensorMap tmW, tmA, tmB;
   const float *pc = a.split;
-  const float *ut = a.split + (size_t)2 * 32 * a.d_out;
+  const void *ut = a.u_planes;
   if (!make_map(&tmW, a.X, (uint64_t)a.d_out, (uint64_t)a.d_in, kTileM) ||
       !make_map(&tmA, pc, (uint64_t)NPL * a.d_out, 32, kTileM) ||
       !make_map(&tmB, ut, (uint64_t)NPL * a.d_in, 32, kTileN))

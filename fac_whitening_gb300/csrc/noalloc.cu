@@ -100,6 +100,7 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.inverse = false;
   a.terms = 3;
   a.split = planes;
+  if (planes) lr_u_planes(f->planes, split, d_out, d_in, &a.u_planes, &a.ut_planes);
   a.codes = static_cast<uint8_t *>(codes);
   a.scales = scales;
   a.amax_out = amax_out;
@@ -107,13 +108,15 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.amax_ws = amax_ws;
   a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + 16);
   if (lr_encode_onepass_ok(L, a, LR_PACK_TENSOR, part, kNoAllocPartFloats)) {
-    if (launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, 2, split) != cudaSuccess) return GIFT_ERR_CUDA;
+    if (!f->planes && launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, 2, split) != cudaSuccess)
+      return GIFT_ERR_CUDA;
     if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
     if (cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return GIFT_ERR_CUDA;
     if (launch_lr_encode_onepass(L, LR_PACK_TENSOR, fmt, a, f->mu, part, Pc) != cudaSuccess) return GIFT_ERR_CUDA;
     return GIFT_OK;
   }
-  if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes) != cudaSuccess)
+  if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes, f->planes) !=
+      cudaSuccess)
     return GIFT_ERR_CUDA;
   if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
   if (lr_encode_fused_ok(L, a, LR_PACK_TENSOR)) {

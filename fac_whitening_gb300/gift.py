@@ -36,7 +36,7 @@ _sz = ctypes.c_size_t
 class GiftFactor(ctypes.Structure):
     _fields_ = [("kind", _i), ("d_in", _i), ("d_out", _i), ("rank", _i),
                 ("U", _vp), ("mu", _vp), ("sigma", _vp),
-                ("LA", _vp), ("LAinv", _vp), ("LG", _vp), ("LGinv", _vp)]
+                ("LA", _vp), ("LAinv", _vp), ("LG", _vp), ("LGinv", _vp), ("planes", _vp)]
 
 
 class GiftError(RuntimeError):
@@ -64,6 +64,8 @@ def _declare(lib):
         "gift_factor_update": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _vp, _i, ctypes.c_uint64, _i,
                                     _vp, _sz, _vp, _vp]),
         "gift_kfac_factor": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
+        "gift_factor_planes_bytes": (_sz, [_i]),
+        "gift_factor_prepare": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp]),
         "gift_amax": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]),
         "gift_encode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                              _vp, _vp, _sz, _vp, _vp]),
@@ -186,14 +188,18 @@ class Factor:
     LAinv: object = None
     LG: object = None
     LGinv: object = None
+    planes: object = None
 
     @staticmethod
-    def empty(kind: str, d_out: int, d_in: int, rank: int = 32, device="cuda") -> "Factor":
+    def empty(kind: str, d_out: int, d_in: int, rank: int = 32, device="cuda", planes: bool = False) -> "Factor":
+        """Zeroed factor buffers; planes=True also allocates the cached U term planes (LOWRANK)."""
         import torch
         f = Factor(kind, d_out, d_in, rank)
         z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)  # noqa: E731
         if kind == "lowrank":
             f.U, f.mu, f.sigma = z(d_in, rank), z(rank), z(1)
+            if planes:
+                f.planes = torch.zeros(lib().gift_factor_planes_bytes(d_in), dtype=torch.uint8, device=device)
         elif kind in ("chol_input", "chol_two_sided"):
             f.LA, f.LAinv = z(d_in, d_in), z(d_in, d_in)
             if kind == "chol_two_sided":
@@ -202,7 +208,7 @@ class Factor:
 
     def c_struct(self) -> GiftFactor:
         return GiftFactor(XFORM[self.kind], self.d_in, self.d_out, self.rank, _p(self.U), _p(self.mu),
-                          _p(self.sigma), _p(self.LA), _p(self.LAinv), _p(self.LG), _p(self.LGinv))
+                          _p(self.sigma), _p(self.LA), _p(self.LAinv), _p(self.LG), _p(self.LGinv), _p(self.planes))
 
 
 def _fptr(f: Optional[Factor]):
@@ -220,6 +226,11 @@ def gift_factor_update(ctx: Context, f: Factor, a, delta=None, seed: int = 0, pr
     _check(lib().gift_factor_update(ctx.handle, ctypes.byref(st), _p(a), a_dt, a.shape[0], _p(delta), d_dt,
                                     seed, PREC[prec], _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                     _p(status), _stream(stream)), "gift_factor_update")
+
+
+def gift_factor_prepare(ctx: Context, f: Factor, stream=None):
+    st = f.c_struct()
+    _check(lib().gift_factor_prepare(ctx.handle, ctypes.byref(st), _stream(stream)), "gift_factor_prepare")
 
 
 def gift_kfac_factor(ctx: Context, a, A_out, prec: str = "fp32", ws=None, status=None, stream=None):

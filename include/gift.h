@@ -109,7 +109,12 @@ typedef enum { GIFT_DT_F32 = 0, GIFT_DT_BF16 = 1 } gift_dtype;
 
 /* One layer's factor: every pointer is device memory owned by the caller.
  *  LOWRANK        : U (d_in x rank, row-major, orthonormal columns), mu (rank values,
- *                   descending, the top eigenvalues of A), sigma (1 value).
+ *                   descending, the top eigenvalues of A), sigma (1 value).  planes
+ *                   (optional, gift_factor_planes_bytes(d_in) bytes, 16-byte aligned): the
+ *                   BF16 term planes of U that the tensor-core kernels read.  When set, the
+ *                   codec reads them instead of rebuilding them on every call; they must
+ *                   then match U: gift_factor_update refreshes them with U, and
+ *                   gift_factor_prepare rebuilds them after the caller changes U.
  *  CHOL_INPUT     : LA and LAinv (d_in x d_in, lower triangular, upper part zero).
  *  CHOL_TWO_SIDED : as CHOL_INPUT plus LG and LGinv (d_out x d_out).
  * Unused pointers may be NULL.  1 <= rank <= 32 and rank <= d_in. */
@@ -121,6 +126,7 @@ typedef struct {
   float *sigma;
   float *LA, *LAinv;
   float *LG, *LGinv;
+  void *planes;
 } gift_factor;
 
 /* Opaque host context: device properties and tuning; holds no device memory and no
@@ -188,6 +194,13 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
 gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
                                const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
                                void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* Bytes of the optional U term planes of a rank-r factor (gift_factor.planes). */
+size_t gift_factor_planes_bytes(int d_in);
+
+/* Rebuild f->planes from f->U (LOWRANK, planes set); asynchronous on `stream`.  Returns
+ * INVALID_ARG when the factor is not LOWRANK or has no U or planes. */
+gift_status gift_factor_prepare(gift_ctx *ctx, const gift_factor *f, cudaStream_t stream);
 
 /* The K-FAC factor alone ([notes] prerequisites, eq. (4): A = a^T a / T), the first step of
  * gift_factor_update, for callers that combine factors before factoring them (for example

@@ -177,3 +177,46 @@ def test_lowrank_amax_matches_transformed(tiny):
     torch.cuda.synchronize()
     out = encode(f, Ws[2], "e4m3")
     assert acc.item() == np.max(np.abs(out["tout"])) == out["amax"][0]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "nvfp4"])
+@pytest.mark.parametrize("prec", ["fp32", "tc"])
+def test_cached_u_planes_match_per_call(c3, fmt, prec):
+    # a factor carrying its U term planes (gift_factor_prepare) gives bit-identical encodes and
+    # decodes to the same factor without them (planes rebuilt inside every call)
+    Ws, F, _ = c3
+    W = Ws[0]
+    d_out, d_in = W.shape
+    f0 = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    f1 = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    f1.planes = torch.zeros(G.lib().gift_factor_planes_bytes(d_in), dtype=torch.uint8, device=DEV)
+    G.gift_factor_prepare(ctx(), f1)
+    e0, e1 = encode(f0, W, fmt, prec=prec), encode(f1, W, fmt, prec=prec)
+    assert e0["status"] == e1["status"] == 0
+    np.testing.assert_array_equal(e0["codes"], e1["codes"])
+    np.testing.assert_array_equal(e0["scales"], e1["scales"])
+    np.testing.assert_array_equal(e0["tout"], e1["tout"])
+    X = t(np.random.default_rng(4).standard_normal(W.shape).astype(np.float32))
+    w = ws("decode", "lowrank", "f32", "tensor", d_out, d_in)
+    outs = []
+    for f in (f0, f1):
+        Wo = torch.empty(d_out, d_in, dtype=torch.float32, device=DEV)
+        G.gift_decode(ctx(), f, X, False, "f32", "tensor", d_out, d_in, Wo, prec=prec, ws=w)
+        torch.cuda.synchronize()
+        outs.append(Wo.cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+def test_factor_update_fills_planes():
+    # gift_factor_update writes the planes together with U; they equal gift_factor_prepare's
+    spec = synth.LayerSpec("m", 128, 1024, T=2048, exponent=1.0, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 9, 4, 1, device="cuda")
+    f = G.Factor.empty("lowrank", 128, 1024, 32, device=DEV, planes=True)
+    n = G.gift_workspace_bytes(ctx(), "factor_update", "lowrank", "e4m3", "tensor", 128, 1024, a.shape[0])
+    G.gift_factor_update(ctx(), f, a, seed=3, ws=torch.zeros(n, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    got = f.planes.clone()
+    f.planes.zero_()
+    G.gift_factor_prepare(ctx(), f)
+    torch.cuda.synchronize()
+    assert torch.equal(got, f.planes) and int(got.count_nonzero()) > 0
