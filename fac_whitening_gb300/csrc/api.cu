@@ -468,6 +468,53 @@ static gift_status codec_common_checks(gift_ctx *ctx, const gift_factor *f, cons
   return check_factor(f, d_out, d_in);
 }
 
+static gift_status encode_checks(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
+                                 gift_format fmt, gift_scaling scaling, const float *residual, const void *codes,
+                                 const void *scales, const float *tensor_scale, const void *ws, size_t ws_bytes) {
+  gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
+  if (cs != GIFT_OK) return cs;
+  if (!codes) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && !tensor_scale) return GIFT_ERR_INVALID_ARG;
+  if (residual == W || codes == (const void *)W) return GIFT_ERR_INVALID_ARG;
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_ENCODE, kind_of(f), d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  return GIFT_OK;
+}
+
+// The one-pass rank-r encode of nb tensors sharing f (per-tensor FP8 or NVFP4, no residual):
+// false when the shape or a pointer does not qualify, with nothing enqueued.
+// amax_only: the same transform, its amax max-accumulated into each item's amax_out (the
+// amax gift_encode would use, for the shapes gift_encode sends here).
+static bool try_onepass(gift_ctx *ctx, const gift_factor *f, int d_out, int d_in, gift_format fmt,
+                        gift_precision prec, const CodecWs &w, const Launch &L, int nb, const LrEncodeItem *items,
+                        gift_status *st, bool amax_only = false) {
+  LrApply o = lr_args(f, items[0].X, d_out, d_in, w, false, prec);
+  o.amax_ws = w.amax;   // one word per tensor, then the grid-barrier counter
+  o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + kOnePassMaxBatch);
+  const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
+  const size_t part_floats = lr_part_floats(ctx->sms, d_out, d_in);
+  for (int k = 0; k < nb; ++k) {
+    LrApply ok = o;
+    ok.X = items[k].X;
+    if (!lr_encode_onepass_ok(L, ok, epi, w.part, part_floats)) return false;
+  }
+  *st = GIFT_OK;
+  cudaError_t e = cudaSuccess;
+  if (!f->planes) e = launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split);
+  for (int k0 = 0; k0 < nb && e == cudaSuccess; k0 += kOnePassMaxBatch) {
+    const int m = (nb - k0 < kOnePassMaxBatch) ? nb - k0 : kOnePassMaxBatch;
+    e = cudaMemsetAsync(w.amax, 0, (kOnePassMaxBatch + 1) * sizeof(float), L.stream);   // amax words + counter
+    if (e == cudaSuccess)
+      e = launch_lr_encode_onepass_batch(L, amax_only ? LR_AMAX : epi, fmt, o, f->mu, w.part, w.Pc, m, items + k0);
+  }
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    *st = GIFT_ERR_CUDA;
+  }
+  return true;
+}
+
 gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in, gift_format fmt,
                       gift_scaling scaling, gift_precision prec, const float *residual, float *amax_accum, void *ws,
                       size_t ws_bytes, int *d_status, cudaStream_t stream) {
@@ -482,6 +529,15 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
   const size_t n = (size_t)d_out * d_in;
   if (kind == GIFT_XF_LOWRANK) {
+    if (!block && !residual) {
+      // the kernel (and so the arithmetic) gift_encode uses for this shape
+      LrEncodeItem it;
+      std::memset(&it, 0, sizeof(it));
+      it.X = W;
+      it.amax_out = amax_accum;
+      gift_status st = GIFT_OK;
+      if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st, true)) return st;
+    }
     CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
     a.R = const_cast<float *>(residual);   // read only by the amax epilogue
@@ -504,15 +560,10 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
                         gift_scaling scaling, gift_precision prec, const float *amax_in, float *residual,
                         void *codes, void *scales, float *tensor_scale, float *transformed_out, float *amax_out,
                         void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
-  gift_status cs = codec_common_checks(ctx, f, W, d_out, d_in, fmt, scaling);
+  gift_status cs = encode_checks(ctx, f, W, d_out, d_in, fmt, scaling, residual, codes, scales, tensor_scale, ws,
+                                 ws_bytes);
   if (cs != GIFT_OK) return cs;
-  if (!codes) return GIFT_ERR_INVALID_ARG;
-  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
-  if (fmt == GIFT_FMT_NVFP4 && !tensor_scale) return GIFT_ERR_INVALID_ARG;
-  if (residual == W || (const void *)codes == (const void *)W) return GIFT_ERR_INVALID_ARG;
   const gift_xform kind = kind_of(f);
-  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
-  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
   const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
   const Launch L = mk(ctx, d_status, stream);
   const size_t n = (size_t)d_out * d_in;
@@ -522,23 +573,16 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
   if (kind == GIFT_XF_LOWRANK) {
     if (fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && block) && !residual) {
       // one pass over W where the shape fits on chip
-      LrApply o = lr_args(f, W, d_out, d_in, w, false, prec);
-      o.tout = transformed_out;
-      o.codes = c8;
-      o.scales = scales;
-      o.tscale = tensor_scale;
-      o.amax_out = amax_out;
-      o.amax_in = amax_in;
-      o.amax_ws = w.amax;
-      o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + 16);
-      const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
-      if (lr_encode_onepass_ok(L, o, epi, w.part, lr_part_floats(ctx->sms, d_out, d_in))) {
-        if (!f->planes) CK(launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split));
-        if (!amax_in) CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
-        CK(cudaMemsetAsync(o.grid_counter, 0, sizeof(unsigned int), stream));
-        CK(launch_lr_encode_onepass(L, epi, fmt, o, f->mu, w.part, w.Pc));
-        return GIFT_OK;
-      }
+      LrEncodeItem it;
+      it.X = W;
+      it.codes = c8;
+      it.scales = scales;
+      it.tscale = tensor_scale;
+      it.amax_out = amax_out;
+      it.tout = transformed_out;
+      it.amax_in = amax_in;
+      gift_status st = GIFT_OK;
+      if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st)) return st;
     }
     CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
@@ -605,6 +649,47 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
   else
     CK(launch_pack_tensor(L, fmt, src, residual, n, amax, c8, static_cast<float *>(scales), amax_out,
                           transformed_out));
+  return GIFT_OK;
+}
+
+gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W, int d_out,
+                                 int d_in, gift_format fmt, gift_scaling scaling, gift_precision prec,
+                                 const float *const *amax_in, void *const *codes, void *const *scales,
+                                 float *const *tensor_scales, float *const *amax_out, void *ws, size_t ws_bytes,
+                                 int *d_status, cudaStream_t stream) {
+  if (!ctx || !W || !codes || R < 1 || R > kMaxReplicas) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && !tensor_scales) return GIFT_ERR_INVALID_ARG;
+  auto at = [](auto arr, int r) { return arr ? arr[r] : nullptr; };
+  // every replica is checked before anything is enqueued
+  for (int r = 0; r < R; ++r) {
+    const gift_status cs = encode_checks(ctx, f, W[r], d_out, d_in, fmt, scaling, nullptr, codes[r], at(scales, r),
+                                         at(tensor_scales, r), ws, ws_bytes);
+    if (cs != GIFT_OK) return cs;
+  }
+  const gift_xform kind = kind_of(f);
+  const Launch L = mk(ctx, d_status, stream);
+  if (kind == GIFT_XF_LOWRANK && fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128)) {
+    const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
+    LrEncodeItem items[kMaxReplicas];
+    for (int r = 0; r < R; ++r) {
+      items[r].X = W[r];
+      items[r].codes = static_cast<uint8_t *>(codes[r]);
+      items[r].scales = at(scales, r);
+      items[r].tscale = at(tensor_scales, r);
+      items[r].amax_out = at(amax_out, r);
+      items[r].tout = nullptr;
+      items[r].amax_in = at(amax_in, r);
+    }
+    gift_status st = GIFT_OK;
+    if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, R, items, &st)) return st;
+  }
+  for (int r = 0; r < R; ++r) {
+    const gift_status st = gift_encode(ctx, f, W[r], d_out, d_in, fmt, scaling, prec, at(amax_in, r), nullptr,
+                                       codes[r], at(scales, r), at(tensor_scales, r), nullptr, at(amax_out, r), ws,
+                                       ws_bytes, d_status, stream);
+    if (st != GIFT_OK) return st;
+  }
   return GIFT_OK;
 }
 

@@ -98,6 +98,19 @@ cudaError_t launch_lr_encode_fused(const Launch &L, int epi, int fmt, const LrAp
 bool lr_encode_onepass_ok(const Launch &L, const LrApply &a, int epi, const float *part, size_t part_floats);
 cudaError_t launch_lr_encode_onepass(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
                                      float *part, float *Pc);
+// One tensor of a batched one-pass encode (tensors that share the factor and the shape).
+struct LrEncodeItem {
+  const float *X;
+  uint8_t *codes;
+  void *scales;
+  float *tscale, *amax_out, *tout;
+  const float *amax_in;
+};
+constexpr int kOnePassMaxBatch = 16;
+// nb <= kOnePassMaxBatch tensors in one launch; a.amax_ws[k] is tensor k's amax word (zero on
+// entry when it has no caller amax).
+cudaError_t launch_lr_encode_onepass_batch(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
+                                           float *part, float *Pc, int nb, const LrEncodeItem *items);
 // lowrank_proj_tc.cu: the projection and the finalize on the tensor cores.  The tensor-core
 // workspace ("split", lr_pipe_split_floats floats) holds, in order: the Pc term planes
 // (2 x d_out rows of 64 BF16), the U term planes for the apply (2 x d_in rows), the U^T term

@@ -219,17 +219,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_lr_proj_tc(const __grid_consta
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const float4 x = *reinterpret_cast<const float4 *>(box + ((lr * 128) + ((c ^ (lr & 7)) << 4)));
-        uint16_t a1, a2, a3, b1, b2, b3;
-        tc::bf16_split3(x.x, a1, a2, a3);
-        tc::bf16_split3(x.y, b1, b2, b3);
-        w1[2 * c] = (uint32_t)a1 | ((uint32_t)b1 << 16);
-        w2[2 * c] = (uint32_t)a2 | ((uint32_t)b2 << 16);
-        w3[2 * c] = (uint32_t)a3 | ((uint32_t)b3 << 16);
-        tc::bf16_split3(x.z, a1, a2, a3);
-        tc::bf16_split3(x.w, b1, b2, b3);
-        w1[2 * c + 1] = (uint32_t)a1 | ((uint32_t)b1 << 16);
-        w2[2 * c + 1] = (uint32_t)a2 | ((uint32_t)b2 << 16);
-        w3[2 * c + 1] = (uint32_t)a3 | ((uint32_t)b3 << 16);
+        tc::bf16_split3x2(x.x, x.y, w1[2 * c], w2[2 * c], w3[2 * c]);
+        tc::bf16_split3x2(x.z, x.w, w1[2 * c + 1], w2[2 * c + 1], w3[2 * c + 1]);
       }
       const uint32_t abase = tmem + lane_off + kPABuf + 96 * b + 16 * half;
       tc::tmem_st16(abase, w1);

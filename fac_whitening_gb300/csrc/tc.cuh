@@ -211,6 +211,21 @@ __device__ __forceinline__ void bf16_split3(float x, uint16_t &t1, uint16_t &t2,
   t2 = __bfloat16_as_ushort(h2);
   t3 = __bfloat16_as_ushort(h3);
 }
+// The same split for two values at once, each term pair packed low = x0, high = x1: one
+// packed conversion per term instead of two (cvt.rn.bf16x2.f32 puts its first source in the
+// upper half), the same roundings and remainders as bf16_split3.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ void bf16_split3x2(float x0, float x1, uint32_t &w1, uint32_t &w2, uint32_t &w3) {
+  w1 = pack_bf16x2_rn(x0, x1);
+  const float r0 = __fsub_rn(x0, __uint_as_float(w1 << 16)), r1 = __fsub_rn(x1, __uint_as_float(w1 & 0xFFFF0000u));
+  w2 = pack_bf16x2_rn(r0, r1);
+  const float s0 = __fsub_rn(r0, __uint_as_float(w2 << 16)), s1 = __fsub_rn(r1, __uint_as_float(w2 & 0xFFFF0000u));
+  w3 = pack_bf16x2_rn(s0, s1);
+}
 // Operand planes of the tensor-core apply, for element (row, k < 32) of a rows x 32 operand:
 // plane 0 row = [t1 of k = 0..31 | t2 of k = 0..31] (128 bytes), plane 1 row = [t3 | zeros].
 // `planes` holds nplanes planes of rows x 64 BF16 each.
@@ -233,14 +248,7 @@ __device__ __forceinline__ void write_term_planes16(uint16_t *planes, size_t row
                                                     int nplanes) {
   uint32_t w1[8], w2[8], w3[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint16_t a1, a2, a3, b1, b2, b3;
-    bf16_split3(x[2 * q], a1, a2, a3);
-    bf16_split3(x[2 * q + 1], b1, b2, b3);
-    w1[q] = (uint32_t)a1 | ((uint32_t)b1 << 16);
-    w2[q] = (uint32_t)a2 | ((uint32_t)b2 << 16);
-    w3[q] = (uint32_t)a3 | ((uint32_t)b3 << 16);
-  }
+  for (int q = 0; q < 8; ++q) bf16_split3x2(x[2 * q], x[2 * q + 1], w1[q], w2[q], w3[q]);
   uint4 *p0 = reinterpret_cast<uint4 *>(planes + row * 64 + kb);
   uint4 *p0b = reinterpret_cast<uint4 *>(planes + row * 64 + 32 + kb);
   p0[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
@@ -288,6 +296,10 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
           smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+// bring a tensor map (kernel parameter or global) into the descriptor cache ahead of its use
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
 }
 // named barrier for a subset of the CTA's warps
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

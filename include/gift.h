@@ -252,6 +252,26 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
                         float *tensor_scale, float *transformed_out, float *amax_out,
                         void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
 
+/* Encode the R data-parallel replicas of one layer's gradient, which share the factor f
+ * ([notes] Algorithm 1, the per-worker encode before AllReduceSum, for R workers modelled on
+ * one GPU).  The result is identical to R gift_encode calls with the same arguments (and
+ * no residual or transformed_out); on the rank-r path with per-tensor FP8 or NVFP4 scaling
+ * the replicas are encoded by one launch per 16 of them, which overlaps the read of one
+ * replica's gradient with the pack of the previous one.
+ *  W, codes, scales, tensor_scales, amax_in, amax_out : host arrays of R device pointers,
+ *              each element as in gift_encode; amax_in and amax_out may be NULL (no
+ *              caller amax / no copy for any replica), tensor_scales may be NULL unless
+ *              fmt is NVFP4, scales may be NULL for F32.
+ *  ws        : one gift_workspace_bytes(GIFT_OP_ENCODE, ...) workspace, used by all replicas
+ *              in stream order.  1 <= R <= 64.  Every replica's arguments are checked
+ *              before anything is enqueued.  d_status: as gift_encode. */
+gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W,
+                                 int d_out, int d_in, gift_format fmt, gift_scaling scaling,
+                                 gift_precision prec, const float *const *amax_in,
+                                 void *const *codes, void *const *scales,
+                                 float *const *tensor_scales, float *const *amax_out, void *ws,
+                                 size_t ws_bytes, int *d_status, cudaStream_t stream);
+
 /* Replica reduce: out = (sum_r deq_r) / R in FP32, adding replicas in order r = 0..R-1
  * with each replica dequantised with its own scale ([notes] eq. (1) data-parallel average;
  * Algorithm 1 AllReduceSum, Dequantize, divide by N — modelled on one GPU over R code

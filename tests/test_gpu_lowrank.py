@@ -169,13 +169,18 @@ def test_lowrank_small_ranks(rank, d_in):
     np.testing.assert_array_equal(out["codes"], O.quantize(out["tout"], "e4m3")["codes"])
 
 
-def test_lowrank_amax_matches_transformed(tiny):
-    Ws, F, _ = tiny
-    f = factor_to_gpu("lowrank", *Ws[0].shape, F=F)
+@pytest.mark.parametrize("which,prec,fmt", [("tiny", "fp32", "e4m3"), ("c3", "fp32", "e4m3"), ("c3", "tc", "e4m3"),
+                                             ("c3", "fp32", "nvfp4")])
+def test_lowrank_amax_matches_transformed(which, prec, fmt, request):
+    # gift_amax returns exactly the amax of the tensor gift_encode quantises (same kernel and
+    # arithmetic for the shape), so a shared amax taken with it never clips an encode
+    Ws, F, _ = request.getfixturevalue(which)
+    W = Ws[-1]
+    f = factor_to_gpu("lowrank", *W.shape, F=F)
     acc = torch.zeros(1, dtype=torch.float32, device=DEV)
-    G.gift_amax(ctx(), f, t(Ws[2]), "e4m3", "tensor", acc, ws=ws("amax", "lowrank", "e4m3", "tensor", *Ws[2].shape))
+    G.gift_amax(ctx(), f, t(W), fmt, "tensor", acc, prec=prec, ws=ws("amax", "lowrank", fmt, "tensor", *W.shape))
     torch.cuda.synchronize()
-    out = encode(f, Ws[2], "e4m3")
+    out = encode(f, W, fmt, prec=prec)
     assert acc.item() == np.max(np.abs(out["tout"])) == out["amax"][0]
 
 
