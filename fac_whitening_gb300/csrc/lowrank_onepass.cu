@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
   // per-tile barriers complete once per tensor (parity = tensor & 1); the rings (U^T planes,
   // A buffers, P accumulators, U planes) count tiles across the whole batch
   __shared__ uint64_t wfull[kOMaxTiles], dfull[2], sdone[kStg];
-  __shared__ uint64_t utfull[2], utempty[2], afull[2], aempty[2], cfull[2], cempty[2];
-  __shared__ uint64_t go2, pcfull, hfree, sfree, dinit, ufull[2], uempty;
+  // mdone[b]: the projection MMAs of the tile in slot b are complete, so its U^T slot and A
+  // buffer are free and its accumulator is ready (one commit serves all three)
+  __shared__ uint64_t utfull[2], mdone[2], afull[2], cempty[2];
+  __shared__ uint64_t go2, pcfull, hfree, sfree, dinit, ufull[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t red[kOWarps];
   __shared__ double coef[32];
@@ -144,17 +146,14 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
     for (int i = 0; i < kStg; ++i) tc::mbar_init(&sdone[i], kOWarps);
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(&utfull[k], 1);
-      tc::mbar_init(&utempty[k], 1);
+      tc::mbar_init(&mdone[k], 1);
       tc::mbar_init(&afull[k], kOWarps);
-      tc::mbar_init(&aempty[k], 1);
-      tc::mbar_init(&cfull[k], 1);
       tc::mbar_init(&cempty[k], kOWarps);
     }
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(&ufull[k], 1);
       tc::mbar_init(&dfull[k], 1);
     }
-    tc::mbar_init(&uempty, 1);
     tc::mbar_init(&go2, 1);
     tc::mbar_init(&pcfull, 1);
     tc::mbar_init(&hfree, kOWarps);
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
         };
         auto load_ut = [&](int i) {
           const int g = g0 + i, u = g & 1;
-          if (!wait(&utempty[u], (uint32_t)(((g >> 1) & 1) ^ 1))) return false;
+          if (!wait(&mdone[u], (uint32_t)(((g >> 1) & 1) ^ 1))) return false;
           tc::mbar_arrive_expect_tx(&utfull[u], NT * kOUtBox);
 #pragma unroll
           for (int t = 0; t < NT; ++t)
@@ -250,7 +249,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
         // once the first group's MMAs are done
         for (int u = 0; u < 2 && u < nt && ok; ++u) {
           const int g = g0 + nt - 1 - u;
-          ok = wait(&utempty[g & 1], (uint32_t)((g >> 1) & 1));
+          ok = wait(&mdone[g & 1], (uint32_t)((g >> 1) & 1));
         }
         for (int i = kOSmemHomes; i < nt && ok; ++i) ok = wait(&sdone[i - kOSmemHomes], kp);
         if (!ok) break;
@@ -262,7 +261,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
 #pragma unroll
         for (int q = 0; q < NPL; ++q) tc::tma_load_2d(sm + kOffPcA + q * kOAPlane, &tmPc, 0, q * d_out + r0, &pcfull);
         if (ngroups == 2 && !kGroupsApart) {
-          if (!wait(&uempty, kp)) break;
+          if (!wait(&dfull[0], kp)) break;   // the first group's MMAs are done with the region
           load_group(1, sm + kOffURing);
         }
       }
@@ -299,9 +298,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
                 tc::mma_bf16_ta(dacc, abuf + 32 * pa[p] + 8 * kk, ub + (uint64_t)((pb[p] * kOUtBox + 32 * kk) / 16),
                                 idesc, (p | kk) ? 1u : 0u);
             }
-            tc::mma_commit(&utempty[b]);
-            tc::mma_commit(&aempty[b]);
-            tc::mma_commit(&cfull[b]);
+            tc::mma_commit(&mdone[b]);
           }
         }
         // phase 2: D = Pc U^T (A = Pc planes, B = U planes), K = 32
@@ -327,7 +324,6 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
               for (int kk = 0; kk < 2; ++kk)
                 tc::mma_bf16(d, pc_desc + (uint64_t)(ao + 2 * kk), b0 + (uint64_t)(bo + 2 * kk), idesc, 1u);
             }
-            if (grp == 0) tc::mma_commit(&uempty);
             tc::mma_commit(&dfull[grp]);
           }
         }
@@ -379,7 +375,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
       for (int j = 0; j < 16; ++j) accp[j] = 0.0f;
       auto fold = [&](int g) {
         const int c = g & 1;
-        wait(&cfull[c], (uint32_t)((g >> 1) & 1));
+        wait(&mdone[c], (uint32_t)((g >> 1) & 1));
         tc::fence_after_sync();
         uint32_t raw[16];
         tc::tmem_ld16_nowait(tmem_k + lane_off + kOTmPAcc + 32 * c + 16 * half, raw);
@@ -393,7 +389,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_lr_encode_onepass(const __grid
       for (int i = 0; i < nt; ++i) {
         const int g = g0 + i, b = g & 1;
         wait(&wfull[i], kp);
-        wait(&aempty[b], (uint32_t)(((g >> 1) & 1) ^ 1));
+        wait(&mdone[b], (uint32_t)(((g >> 1) & 1) ^ 1));
         tc::fence_after_sync();
         const uint8_t *box = (i < kOSmemHomes ? sm + kOffHome + i * kOTile : sm + kOffStage + (i & 1) * kOTile) +
                              half * kOBox;
