@@ -102,13 +102,13 @@ def profiled_traffic(group):
     when the kernel source has changed since the counters were taken."""
     import hashlib
     import re
-    path = os.path.join(ROOT, "profiles", "onepass_encode_1536x6144.md")
+    path = os.path.join(ROOT, "profiles", "encode_batch_1536x6144.md")
     if group != "gift_encode" or not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    src = os.path.join(ROOT, "fac_whitening_gb300", "csrc", "lowrank_onepass.cu")
+    src = os.path.join(ROOT, "fac_whitening_gb300", "csrc", "lowrank_batch.cu")
     if not (m_src and m_b and os.path.exists(src)):
         return None
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_src.group(1):
@@ -458,10 +458,10 @@ def main_gift(args):
     value = job_value(world, grad_bytes, ms)
 
     # ---- roofline of the dominant kernel ----------------------------------------------
-    # The dominant group is normally the rank-r encode: one cooperative one-pass launch per
-    # layer encodes its R replicas.  Its launch duration is timed on its own: the group's
-    # calls replayed back to back on one stream (CUDA events around the replays), so calls
-    # do not overlap.
+    # The dominant group is normally the rank-r encode: one gift_encode_replicas call per
+    # layer encodes its R replicas (projection pass, Pc reduce, apply-and-pack pass).  Its
+    # call duration is timed on its own: the group's calls replayed back to back on one
+    # stream (CUDA events around the replays), so calls do not overlap.
     dom = max(group_ms, key=group_ms.get)
     bytes_g, launches_g, calls_g = alg[dom]
     solo = solo_call_ms(graphs_solo.get(dom), calls_g, args.steps) if graphs_solo.get(dom) else None

@@ -42,6 +42,8 @@ struct CodecWs {
   float *xbuf = nullptr;   // transformed tensor (CHOL encode) or dequantised input (decode)
   float *tbuf = nullptr;   // CHOL_TWO_SIDED intermediate
   float *split = nullptr;  // LOWRANK: tensor-core operand planes and counters (kernels.cuh)
+  float *bpart = nullptr;  // LOWRANK, batched encode: kBatchWs x lr_batch_part_floats
+  uint16_t *bplanes = nullptr;   // LOWRANK, batched encode: kBatchWs x 2 x d_out rows of 64 BF16
   int nsplit = 0;
   size_t bytes = 0;
 };
@@ -56,6 +58,11 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
     w.part = c.take<float>(lr_part_floats(sms, d_out, d_in));
     w.Pc = c.take<float>((size_t)d_out * 32);
     w.split = c.take<float>(lr_pipe_split_floats(d_out, d_in));
+    const size_t bp = lr_batch_part_floats(sms, d_out, d_in);
+    if (bp && (op == GIFT_OP_ENCODE || op == GIFT_OP_AMAX)) {
+      w.bpart = c.take<float>((size_t)kBatchWs * bp);
+      w.bplanes = c.take<uint16_t>((size_t)kBatchWs * 2 * d_out * 64);
+    }
   }
   if (kind != GIFT_XF_IDENTITY) {
     if (op == GIFT_OP_DECODE || kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED)
@@ -482,31 +489,31 @@ static gift_status encode_checks(gift_ctx *ctx, const gift_factor *f, const floa
   return GIFT_OK;
 }
 
-// The one-pass rank-r encode of nb tensors sharing f (per-tensor FP8 or NVFP4, no residual):
+// The batched rank-r encode of nb tensors sharing f (per-tensor FP8 or NVFP4, no residual):
 // false when the shape or a pointer does not qualify, with nothing enqueued.
 // amax_only: the same transform, its amax max-accumulated into each item's amax_out (the
 // amax gift_encode would use, for the shapes gift_encode sends here).
-static bool try_onepass(gift_ctx *ctx, const gift_factor *f, int d_out, int d_in, gift_format fmt,
+static bool try_batch(gift_ctx *ctx, const gift_factor *f, int d_out, int d_in, gift_format fmt,
                         gift_precision prec, const CodecWs &w, const Launch &L, int nb, const LrEncodeItem *items,
                         gift_status *st, bool amax_only = false) {
+  if (!w.bpart || !w.bplanes) return false;
   LrApply o = lr_args(f, items[0].X, d_out, d_in, w, false, prec);
   o.amax_ws = w.amax;   // one word per tensor, then the grid-barrier counter
-  o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + kOnePassMaxBatch);
+  o.grid_counter = reinterpret_cast<unsigned int *>(w.amax + kEncodeBatchMax);
   const int epi = (fmt == GIFT_FMT_NVFP4) ? LR_NVFP4 : LR_PACK_TENSOR;
-  const size_t part_floats = lr_part_floats(ctx->sms, d_out, d_in);
   for (int k = 0; k < nb; ++k) {
     LrApply ok = o;
     ok.X = items[k].X;
-    if (!lr_encode_onepass_ok(L, ok, epi, w.part, part_floats)) return false;
+    if (!lr_encode_batch_ok(L, ok, epi)) return false;
   }
   *st = GIFT_OK;
   cudaError_t e = cudaSuccess;
   if (!f->planes) e = launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, prec == GIFT_PREC_TC ? 1 : 2, w.split);
-  for (int k0 = 0; k0 < nb && e == cudaSuccess; k0 += kOnePassMaxBatch) {
-    const int m = (nb - k0 < kOnePassMaxBatch) ? nb - k0 : kOnePassMaxBatch;
-    e = cudaMemsetAsync(w.amax, 0, (kOnePassMaxBatch + 1) * sizeof(float), L.stream);   // amax words + counter
+  for (int k0 = 0; k0 < nb && e == cudaSuccess; k0 += kBatchWs) {
+    const int m = (nb - k0 < kBatchWs) ? nb - k0 : kBatchWs;
+    e = cudaMemsetAsync(w.amax, 0, (kEncodeBatchMax + 1) * sizeof(float), L.stream);   // amax words + counter
     if (e == cudaSuccess)
-      e = launch_lr_encode_onepass_batch(L, amax_only ? LR_AMAX : epi, fmt, o, f->mu, w.part, w.Pc, m, items + k0);
+      e = launch_lr_encode_batch(L, amax_only ? LR_AMAX : epi, fmt, o, f->mu, w.bpart, w.bplanes, m, items + k0);
   }
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -536,7 +543,7 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
       it.X = W;
       it.amax_out = amax_accum;
       gift_status st = GIFT_OK;
-      if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st, true)) return st;
+      if (try_batch(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st, true)) return st;
     }
     CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
@@ -572,7 +579,8 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
 
   if (kind == GIFT_XF_LOWRANK) {
     if (fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && block) && !residual) {
-      // one pass over W where the shape fits on chip
+      // the batched kernels (projection pass, then apply and pack with the tensor on chip)
+      // where the shape fits
       LrEncodeItem it;
       it.X = W;
       it.codes = c8;
@@ -582,7 +590,7 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
       it.tout = transformed_out;
       it.amax_in = amax_in;
       gift_status st = GIFT_OK;
-      if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st)) return st;
+      if (try_batch(ctx, f, d_out, d_in, fmt, prec, w, L, 1, &it, &st)) return st;
     }
     CK(lr_prepare(L, f, W, d_out, d_in, w, false, prec));
     LrApply a = lr_args(f, W, d_out, d_in, w, false, prec);
@@ -682,7 +690,7 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
       items[r].amax_in = at(amax_in, r);
     }
     gift_status st = GIFT_OK;
-    if (try_onepass(ctx, f, d_out, d_in, fmt, prec, w, L, R, items, &st)) return st;
+    if (try_batch(ctx, f, d_out, d_in, fmt, prec, w, L, R, items, &st)) return st;
   }
   for (int r = 0; r < R; ++r) {
     const gift_status st = gift_encode(ctx, f, W[r], d_out, d_in, fmt, scaling, prec, at(amax_in, r), nullptr,

@@ -92,13 +92,7 @@ cudaError_t launch_lr_apply_tc(const Launch &L, int epi, int fmt, const LrApply 
 // on shapes whose tiles fit in tensor memory across the SMs; cooperative launch.
 bool lr_encode_fused_ok(const Launch &L, const LrApply &a, int epi);
 cudaError_t launch_lr_encode_fused(const Launch &L, int epi, int fmt, const LrApply &a);
-// lowrank_onepass.cu: projection, Pc, transform, grid-wide amax and pack in one cooperative
-// kernel (W read once).  Needs the U planes in a.split (launch_lr_split_u_all), a.amax_ws
-// zeroed (without a caller amax) and a.grid_counter zeroed.
-bool lr_encode_onepass_ok(const Launch &L, const LrApply &a, int epi, const float *part, size_t part_floats);
-cudaError_t launch_lr_encode_onepass(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
-                                     float *part, float *Pc);
-// One tensor of a batched one-pass encode (tensors that share the factor and the shape).
+// One tensor of a batched rank-r encode (tensors that share the factor and the shape).
 struct LrEncodeItem {
   const float *X;
   uint8_t *codes;
@@ -106,11 +100,20 @@ struct LrEncodeItem {
   float *tscale, *amax_out, *tout;
   const float *amax_in;
 };
-constexpr int kOnePassMaxBatch = 16;
-// nb <= kOnePassMaxBatch tensors in one launch; a.amax_ws[k] is tensor k's amax word (zero on
-// entry when it has no caller amax).
-cudaError_t launch_lr_encode_onepass_batch(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
-                                           float *part, float *Pc, int nb, const LrEncodeItem *items);
+constexpr int kEncodeBatchMax = 16;   // tensors per batched launch; the amax words precede the
+                                      // grid-barrier word (at index kEncodeBatchMax)
+// Tensors per batched launch that the codec workspace holds partials for.
+constexpr int kBatchWs = 8;
+// lowrank_batch.cu: the rank-r encode of up to kEncodeBatchMax tensors sharing a factor, in
+// two streaming passes (projection of every tensor, then apply, tensor amax and pack with the
+// tensor in tensor memory).  Needs the U planes (a.u_planes, a.ut_planes), a.amax_ws[0..nb)
+// zeroed for the tensors without a caller amax, a.grid_counter zeroed; part holds nb x
+// lr_batch_part_floats floats and pc_planes nb x 2 x d_out rows of 64 BF16.
+int lr_batch_plan(int sms, int d_out, int d_in, int *cpr_out);
+size_t lr_batch_part_floats(int sms, int d_out, int d_in);
+bool lr_encode_batch_ok(const Launch &L, const LrApply &a, int epi);
+cudaError_t launch_lr_encode_batch(const Launch &L, int epi, int fmt, const LrApply &a, const float *mu,
+                                   float *part, uint16_t *pc_planes, int nb, const LrEncodeItem *items);
 // lowrank_proj_tc.cu: the projection and the finalize on the tensor cores.  The tensor-core
 // workspace ("split", lr_pipe_split_floats floats) holds, in order: the Pc term planes
 // (2 x d_out rows of 64 BF16), the U term planes for the apply (2 x d_in rows), the U^T term

@@ -107,12 +107,21 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.amax_in = amax_in;
   a.amax_ws = amax_ws;
   a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + 16);
-  if (lr_encode_onepass_ok(L, a, LR_PACK_TENSOR, part, kNoAllocPartFloats)) {
+  if (lr_encode_batch_ok(L, a, LR_PACK_TENSOR) && lr_batch_part_floats(ctx->sms, d_out, d_in) <= kNoAllocPartFloats) {
     if (!f->planes && launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, 2, split) != cudaSuccess)
       return GIFT_ERR_CUDA;
-    if (!amax_in && cudaMemsetAsync(amax_ws, 0, sizeof(float), stream) != cudaSuccess) return GIFT_ERR_CUDA;
-    if (cudaMemsetAsync(a.grid_counter, 0, sizeof(unsigned int), stream) != cudaSuccess) return GIFT_ERR_CUDA;
-    if (launch_lr_encode_onepass(L, LR_PACK_TENSOR, fmt, a, f->mu, part, Pc) != cudaSuccess) return GIFT_ERR_CUDA;
+    // the amax words and the grid-barrier word
+    if (cudaMemsetAsync(amax_ws, 0, (kEncodeBatchMax + 1) * sizeof(float), stream) != cudaSuccess)
+      return GIFT_ERR_CUDA;
+    LrEncodeItem it{};
+    it.X = W;
+    it.codes = a.codes;
+    it.scales = a.scales;
+    it.amax_out = amax_out;
+    it.amax_in = amax_in;
+    if (launch_lr_encode_batch(L, LR_PACK_TENSOR, fmt, a, f->mu, part, lr_planes(split, d_out, d_in).pc, 1, &it) !=
+        cudaSuccess)
+      return GIFT_ERR_CUDA;
     return GIFT_OK;
   }
   if (lr_prepare_all(L, f->U, f->mu, f->sigma, f->rank, W, d_out, d_in, false, false, part, Pc, planes, f->planes) !=
