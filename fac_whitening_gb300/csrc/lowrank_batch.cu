@@ -23,7 +23,8 @@
 //          clock-bounded grid barrier gives the tensor amax, and the pack reads tensor memory
 //          and stores the codes through shared memory as coalesced rows.  A home (tile) of
 //          tensor memory takes the next tensor's alpha W as soon as its codes are packed, and
-//          the next tensor's first tiles are already in the ring by then.
+//          the next tensor's first tiles are already in the ring by then.  The tensors are
+//          taken last to first: the last ones pass A read are still in L2.
 // W is read twice (pass A and pass B) but neither pass waits on the other tensors.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -72,6 +73,7 @@ struct BatchMaps {
 struct ApplyBatchParams {
   LrApply a;                 // factor, planes, shapes; a.amax_ws = one word per tensor
   int tiles_n, cpr, nb;
+  int reverse;               // take the tensors last to first (the last ones projected are still in L2)
   unsigned int *grid_counter;   // zero on entry
   LrEncodeItem item[kEncodeBatchMax];
 };
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
   const int ngroups = nt > kBGroupTiles ? 2 : 1;
   const int ntile0 = nt < kBGroupTiles ? nt : kBGroupTiles;   // tiles of the first group
   const unsigned int G = gridDim.x;
+  auto tix = [&](int k) { return P.reverse ? P.nb - 1 - k : k; };   // tensor at position k
 
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base_sh, 512);
@@ -424,8 +427,9 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
         if (g >= kBStages && !wait(&sempty[s], (uint32_t)(((g / kBStages) - 1) & 1))) return false;
         uint8_t *dst = sm + s * kBTile;
         tc::mbar_arrive_expect_tx(&sfull[s], kBTile);
-        tc::tma_load_2d(dst, &M.w[k], (B.cb0 + i) * kBN, B.r0, &sfull[s]);
-        tc::tma_load_2d(dst + kBBox, &M.w[k], (B.cb0 + i) * kBN + 32, B.r0, &sfull[s]);
+        const CUtensorMap *mw = &M.w[tix(k)];
+        tc::tma_load_2d(dst, mw, (B.cb0 + i) * kBN, B.r0, &sfull[s]);
+        tc::tma_load_2d(dst + kBBox, mw, (B.cb0 + i) * kBN + 32, B.r0, &sfull[s]);
         return true;
       };
       // a group's U planes: one 256-row box per plane (rows past the CTA's tiles unused)
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
         tc::mbar_arrive_expect_tx(&pcfull, NPL * kBPcPlane);
 #pragma unroll
         for (int q = 0; q < NPL; ++q)
-          tc::tma_load_2d(sm + kBOffPc + q * kBPcPlane, &tmPc, 0, (2 * k + q) * d_out + B.r0, &pcfull);
+          tc::tma_load_2d(sm + kBOffPc + q * kBPcPlane, &tmPc, 0, (2 * tix(k) + q) * d_out + B.r0, &pcfull);
         if (ngroups == 2) {
           if (!wait(&dfull[0], kp)) break;   // the first group's MMAs are done with the region
           load_group(1);
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
       const uint32_t home0 = tmem_k + lane_off + (uint32_t)(32 * half);
       auto slot = [&](int i) { return home0 + (uint32_t)(kBN * i); };
-      const LrEncodeItem &it = P.item[k];
+      const LrEncodeItem &it = P.item[tix(k)];
       const uint32_t kp = (uint32_t)(k & 1);
 
       // ---------------- alpha W of the second group (the first one moved during the last pack) ----------------
@@ -608,7 +612,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
         if (it.amax_in) {
           amax = it.amax_in[0];
         } else {
-          unsigned int *word = reinterpret_cast<unsigned int *>(a.amax_ws) + k;
+          unsigned int *word = reinterpret_cast<unsigned int *>(a.amax_ws) + tix(k);
           // no return value needed: ordered before the barrier's release by program order
           if (m) asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(word), "r"(m) : "memory");
           grid_barrier();
@@ -885,6 +889,7 @@ cudaError_t launch_lr_encode_batch(const Launch &L, int epi, int fmt, const LrAp
   PB.tiles_n = PA.tiles_n;
   PB.cpr = cpr;
   PB.nb = nb;
+  PB.reverse = 1;
   PB.grid_counter = a.grid_counter;
   for (int k = 0; k < nb; ++k) PB.item[k] = items[k];
   return NPL == 1 ? apply_dispatch<1>(L, epi, fmt, PB, M, tmU, tmPc, grid, tout)

@@ -256,8 +256,9 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
  * ([notes] Algorithm 1, the per-worker encode before AllReduceSum, for R workers modelled on
  * one GPU).  The result is identical to R gift_encode calls with the same arguments (and
  * no residual or transformed_out); on the rank-r path with per-tensor FP8 or NVFP4 scaling
- * the replicas are encoded by one launch per 16 of them, which overlaps the read of one
- * replica's gradient with the pack of the previous one.
+ * each group of up to 8 replicas is encoded by three launches (projection of every replica,
+ * Pc, then apply and pack), which overlap the read of one replica's gradient with the pack
+ * of the previous one.
  *  W, codes, scales, tensor_scales, amax_in, amax_out : host arrays of R device pointers,
  *              each element as in gift_encode; amax_in and amax_out may be NULL (no
  *              caller amax / no copy for any replica), tensor_scales may be NULL unless
