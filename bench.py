@@ -97,18 +97,27 @@ def solo_call_ms(graph, calls, reps):
     return a.elapsed_time(b) / max(1, reps) / calls
 
 
+# stage group -> (ncu summary under profiles/, the kernel source its counters belong to)
+PROFILES = {"gift_encode": ("encode_batch_1536x6144.md", "lowrank_batch.cu"),
+            "euclid_encode": ("pack_tensor_600m_shapes.md", "quant.cu"),
+            "euclid_amax": ("pack_tensor_600m_shapes.md", "quant.cu")}
+
+
 def profiled_traffic(group):
-    """DRAM bytes per launch of the group's kernel from the committed ncu summary, or None
-    when the kernel source has changed since the counters were taken."""
+    """DRAM bytes per call of the group from the committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
     import hashlib
     import re
-    path = os.path.join(ROOT, "profiles", "encode_batch_1536x6144.md")
-    if group != "gift_encode" or not os.path.exists(path):
+    if group not in PROFILES:
+        return None
+    name, source = PROFILES[group]
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    src = os.path.join(ROOT, "fac_whitening_gb300", "csrc", "lowrank_batch.cu")
+    m_b = re.search(group + r"_traffic_bytes_per_call:\s*([0-9]+)", text)
+    src = os.path.join(ROOT, "fac_whitening_gb300", "csrc", source)
     if not (m_src and m_b and os.path.exists(src)):
         return None
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_src.group(1):
@@ -339,9 +348,16 @@ def main_gift(args):
         E["avg"] = torch.empty(E["spec"].d_out, E["spec"].d_in, dtype=torch.float32, device=dev)
         E["shared"] = shared[j:j + 1]
 
+    solo_mode = [False]
+
     def fork_join(items, fn):
         """Run fn(item, ws) for independent items round-robin over the side streams; the
-        current stream waits for all of them (one join per stage group)."""
+        current stream waits for all of them (one join per stage group).  In solo mode the
+        items run back to back on the current stream (per-call timing)."""
+        if solo_mode[0]:
+            for it in items:
+                fn(it, wss[0])
+            return
         main = torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(main)
@@ -415,15 +431,16 @@ def main_gift(args):
                 fn()
             graphs.append((name, g))
     torch.cuda.synchronize()
-    # the dominant group's calls on a single stream, for the per-launch roofline timing
+    # every group's calls back to back on a single stream, for the per-call roofline timing
     graphs_solo = {}
-    if gl:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
+    solo_mode[0] = True
+    with torch.cuda.stream(cap):
+        for name, fn in groups:
+            g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                for f, L in zip(factors, gl):
-                    encode_layer(f, L, wss[0])
-        graphs_solo["gift_encode"] = g
+                fn()
+            graphs_solo[name] = g
+    solo_mode[0] = False
     torch.cuda.synchronize()
 
     def step(evs=None):

@@ -15,16 +15,18 @@
 //          the stacked U^T terms ([u1;u2;u3], [u1;u2], [u1]), so that the six products
 //          x_i u_j (i + j <= 2) land in three 32-column groups of a fresh accumulator per tile;
 //          the groups are added and folded into the slice sum with round-to-nearest FP32 adds.
-//   reduce (k_lr_pc_batch): Pc = c * (sum over the slices, slice order, compensated FP32; c in
-//          FP64), as BF16 term planes.
-//   pass B (k_lr_apply_batch, cooperative): W~ of the whole CTA block in tensor memory
-//          (8 tiles x 64 columns): the W tiles stream through a 4-deep ring into alpha W in
-//          tensor memory, two N = 256 MMA chains add Pc U^T, the workers take the amax, one
-//          clock-bounded grid barrier gives the tensor amax, and the pack reads tensor memory
-//          and stores the codes through shared memory as coalesced rows.  A home (tile) of
-//          tensor memory takes the next tensor's alpha W as soon as its codes are packed, and
-//          the next tensor's first tiles are already in the ring by then.  The tensors are
-//          taken last to first: the last ones pass A read are still in L2.
+//   reduce (k_lr_pc_batch): Pc / alpha = (c / alpha) * (sum over the slices, slice order,
+//          compensated FP32; c / alpha = (sigma / mu)^1/2 - 1 in FP64), as BF16 term planes.
+//   pass B (k_lr_apply_batch, cooperative): D = W + (Pc / alpha) U^T of the whole CTA block
+//          in tensor memory (8 tiles x 64 columns), W~ = alpha D.  The W tiles stream through a
+//          3-deep TMA ring and the tensor core copies them into tensor memory (tcgen05.cp);
+//          two N = 256 MMA chains add (Pc / alpha) U^T; the workers take the amax of alpha D,
+//          one clock-bounded grid barrier gives the tensor amax, and the pack reads tensor
+//          memory and stores the codes through shared memory as coalesced rows.  A group of
+//          tensor memory takes the next tensor's W as soon as its codes are packed, the next
+//          tensor's first tiles already waiting in the ring; its Pc and U planes load as soon
+//          as this tensor's MMAs are done.  The tensors are taken last to first: the last
+//          ones pass A read are still in L2.
 // W is read twice (pass A and pass B) but neither pass waits on the other tensors.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -55,13 +57,14 @@ constexpr long long kBWait = 4000000000LL;
 constexpr int kAOffUt = 0;
 constexpr int kAOffStage = kBMaxTiles * 3 * kBUtPlane;                // 96 KB
 constexpr int kASmem = kAOffStage + kBStages * kBTile;                // 224 KB
-// pass B shared memory: the W ring, the Pc planes (code staging during the pack), a group's
-// U planes
-constexpr int kBOffPc = kBStages * kBTile;                            // 128 KB
-constexpr int kBOffU = kBOffPc + 2 * kBPcPlane;                       // 160 KB
-constexpr int kBSmem = kBOffU + 2 * kBUGroup;                         // 224 KB
+// pass B shared memory: a 3-deep W ring, the Pc planes, a group's U planes, code staging
+constexpr int kBRing = 3;
+constexpr int kBOffPc = kBRing * kBTile;                              // 96 KB
+constexpr int kBOffU = kBOffPc + 2 * kBPcPlane;                       // 128 KB
+constexpr int kBOffStg = kBOffU + 2 * kBUGroup;                       // 192 KB
+constexpr int kBStg = 128 * 256;                                      // a group's FP8 code rows
+constexpr int kBSmem = kBOffStg + kBStg;                              // 224 KB
 constexpr int kBOffScales = 128 * 128;   // NVFP4 staging: block scales after the code rows
-static_assert(128 * 256 <= 2 * kBPcPlane, "FP8 code staging of a group outside the Pc region");
 
 struct ProjBatchParams {
   int d_out, d_in, tiles_n, cpr, nb;
@@ -299,7 +302,8 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_proj_batch(const __grid_con
 }
 
 // ---------------------------------------------------------------------------------------
-// reduce: Pc of every tensor from its slice partials, written as BF16 term planes
+// reduce: Pc / alpha (alpha = sigma^-1/2) of every tensor from its slice partials, written as
+// BF16 term planes
 template <int NPL>
 __global__ void __launch_bounds__(256) k_lr_pc_batch(const float *__restrict__ part, int nb, int cpr, int d_out,
                                                      const float *__restrict__ mu, const float *__restrict__ sigma,
@@ -313,19 +317,19 @@ __global__ void __launch_bounds__(256) k_lr_pc_batch(const float *__restrict__ p
       if (!(m > 0.0) || !(sg > 0.0)) {
         if (blockIdx.x == 0) set_status(status, GIFT_ERR_NOT_PD);
       } else {
-        c = 1.0 / sqrt(m) - 1.0 / sqrt(sg);
+        c = (1.0 / sqrt(m) - 1.0 / sqrt(sg)) * sqrt(sg);   // c / alpha: pass B adds onto W
       }
     }
     cf[k] = c;
   }
   __syncthreads();
+  // thread = (tensor, row, 2 consecutive columns); the planes take one 4-byte store per term
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per = (long long)d_out * 16;
   if (item >= per * nb) return;
   const int k = (int)(item / per);
   const int rem = (int)(item - (long long)k * per);
   const int row = rem >> 4, kb = 2 * (rem & 15);
-  const double coef[2] = {cf[kb], cf[kb + 1]};
   float sum[2] = {0.f, 0.f}, comp[2] = {0.f, 0.f};
   const float *src = part + ((size_t)k * cpr * d_out + row) * 32 + kb;
   for (int q0 = 0; q0 < cpr; q0 += 16) {
@@ -346,16 +350,22 @@ __global__ void __launch_bounds__(256) k_lr_pc_batch(const float *__restrict__ p
         }
       }
   }
-  uint16_t *planes = pc_planes + (size_t)k * 2 * d_out * 64;
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const float pc = (float)(coef[e] * ((double)sum[e] - (double)comp[e]));
-    tc::write_term_planes(planes, (size_t)d_out, (size_t)row, kb + e, pc, NPL);
+  const float p0 = (float)(cf[kb] * ((double)sum[0] - (double)comp[0]));
+  const float p1 = (float)(cf[kb + 1] * ((double)sum[1] - (double)comp[1]));
+  uint32_t t1, t2, t3;
+  tc::bf16_split3x2(p0, p1, t1, t2, t3);
+  // planes of tensor k: plane 0 rows [t1 | t2], plane 1 rows [t3 | 0] (64 BF16 each)
+  uint16_t *q = pc_planes + (size_t)k * 2 * d_out * 64 + (size_t)row * 64;
+  *reinterpret_cast<uint32_t *>(q + kb) = t1;
+  *reinterpret_cast<uint32_t *>(q + 32 + kb) = t2;
+  if (NPL > 1) {
+    *reinterpret_cast<uint32_t *>(q + (size_t)d_out * 64 + kb) = t3;
+    *reinterpret_cast<uint32_t *>(q + (size_t)d_out * 64 + 32 + kb) = 0u;
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// pass B: W~ = alpha W + Pc U^T held in tensor memory, tensor amax, pack
+// pass B: D = W + (Pc / alpha) U^T held in tensor memory, W~ = alpha D, tensor amax, pack
 template <int EPI, int F, int NPL, bool TOUT>
 __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_constant__ ApplyBatchParams P,
                                                                  const __grid_constant__ BatchMaps M,
@@ -366,7 +376,8 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023);
   // per-tensor barriers complete once per tensor (parity = tensor & 1); the ring counts tiles
   // across the batch
-  __shared__ uint64_t sfull[kBStages], sempty[kBStages], pcfull, ufull[2], hready[2], dfull[2], cfree;
+  // hfree[grp]: the previous tensor's codes of group grp are packed, its tensor memory is free
+  __shared__ uint64_t sfull[kBRing], sempty[kBRing], pcfull, ufull[2], hfree[2], dfull[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t red[kBWarps];
   __shared__ float amax_sh;
@@ -387,17 +398,16 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
     tc::tmem_relinquish();
   }
   if (tid == 32) {
-    for (int s = 0; s < kBStages; ++s) {
+    for (int s = 0; s < kBRing; ++s) {
       tc::mbar_init(&sfull[s], 1);
-      tc::mbar_init(&sempty[s], kBWarps);
+      tc::mbar_init(&sempty[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(&ufull[k], 1);
-      tc::mbar_init(&hready[k], kBWarps);
+      tc::mbar_init(&hfree[k], kBWarps);
       tc::mbar_init(&dfull[k], 1);
     }
     tc::mbar_init(&pcfull, 1);
-    tc::mbar_init(&cfree, kBWarps);
     tc::fence_mbar_init();
     failed = 0;
   }
@@ -423,8 +433,8 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       tc::prefetch_tensormap(&tmPc);
       for (int k = 0; k < P.nb; ++k) tc::prefetch_tensormap(&M.w[k]);
       auto load_w = [&](int k, int i) {
-        const int g = k * nt + i, s = g & (kBStages - 1);
-        if (g >= kBStages && !wait(&sempty[s], (uint32_t)(((g / kBStages) - 1) & 1))) return false;
+        const int g = k * nt + i, s = g % kBRing;
+        if (g >= kBRing && !wait(&sempty[s], (uint32_t)(((g / kBRing) - 1) & 1))) return false;
         uint8_t *dst = sm + s * kBTile;
         tc::mbar_arrive_expect_tx(&sfull[s], kBTile);
         const CUtensorMap *mw = &M.w[tix(k)];
@@ -442,18 +452,18 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       };
       for (int k = 0; k < P.nb; ++k) {
         const uint32_t kp = (uint32_t)(k & 1), pp = kp ^ 1u;
-        bool ok = true;
-        for (int i = 0; i < ntile0 && ok; ++i) ok = load_w(k, i);
-        // the first group's U planes once the previous tensor's last group is done with them
-        if (!ok || (k > 0 && !wait(&dfull[ngroups - 1], pp))) break;
+        // the first group's U planes and the Pc planes as soon as the previous tensor's MMAs
+        // are done with their regions, ahead of this tensor's W tiles (which wait for ring
+        // slots and queue in the same TMA unit)
+        if (k > 0 && !wait(&dfull[ngroups - 1], pp)) break;
         load_group(0);
-        for (int i = ntile0; i < nt && ok; ++i) ok = load_w(k, i);
-        // Pc once the previous tensor's codes have left its region
-        if (!ok || (k > 0 && !wait(&cfree, pp))) break;
         tc::mbar_arrive_expect_tx(&pcfull, NPL * kBPcPlane);
 #pragma unroll
         for (int q = 0; q < NPL; ++q)
           tc::tma_load_2d(sm + kBOffPc + q * kBPcPlane, &tmPc, 0, (2 * tix(k) + q) * d_out + B.r0, &pcfull);
+        bool ok = true;
+        for (int i = 0; i < nt && ok; ++i) ok = load_w(k, i);
+        if (!ok) break;
         if (ngroups == 2) {
           if (!wait(&dfull[0], kp)) break;   // the first group's MMAs are done with the region
           load_group(1);
@@ -462,21 +472,40 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
     }
   } else if (warp == kBWarps + 1) {
     // ======================= MMA issuer =======================
+    // Per group: each W tile is copied from the ring into its tensor-memory home
+    // (tcgen05.cp, 8 copies of 128 rows x 32 bytes), then one N = 256 MMA chain adds
+    // (Pc / alpha) U^T onto the group's tiles (copies and MMAs run in issue order).
     if (lane == 0) {
       const uint64_t pc0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sm + kBOffPc));
       const uint64_t u0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sm + kBOffU));
+      const uint64_t w0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sm));
       constexpr int np = (NPL == 1) ? 3 : 6;
       constexpr int pa[6] = {NPL == 1 ? 1 : 2, NPL == 1 ? 0 : 1, 0, 1, 0, 0};
       constexpr int pb[6] = {0, 1, NPL == 1 ? 0 : 2, 0, 1, 0};
       for (int k = 0; k < P.nb && !failed; ++k) {
-        const uint32_t kp = (uint32_t)(k & 1);
-        if (!wait(&pcfull, kp)) break;
+        const uint32_t kp = (uint32_t)(k & 1), pp = kp ^ 1u;
         for (int grp = 0; grp < ngroups; ++grp) {
-          if (!wait(&ufull[grp], kp) || !wait(&hready[grp], kp)) break;
+          if (k > 0 && !wait(&hfree[grp], pp)) break;   // the previous tensor's codes are out
+          const int i0 = kBGroupTiles * grp, i1 = grp == 0 ? ntile0 : nt;
+          bool ok = true;
+          for (int i = i0; i < i1 && ok; ++i) {
+            const int g = k * nt + i, s = g % kBRing;
+            if (!(ok = wait(&sfull[s], (uint32_t)((g / kBRing) & 1)))) break;
+            tc::fence_after_sync();
+            const uint64_t ws = w0 + (uint64_t)(s * kBTile / 16);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)      // the tile's two 32-column boxes
+#pragma unroll
+              for (int j = 0; j < 4; ++j)    // 8 columns per copy
+                tc::cp_128x256b(tmem + (uint32_t)(kBN * i + 32 * h + 8 * j),
+                                ws + (uint64_t)((h * kBBox + 32 * j) / 16));
+            tc::mma_commit(&sempty[s]);
+          }
+          if (!ok || (grp == 0 && !wait(&pcfull, kp)) || !wait(&ufull[grp], kp)) break;
           tc::fence_after_sync();
-          const int ntile = grp == 0 ? ntile0 : nt - kBGroupTiles;
+          const int ntile = i1 - i0;
           const uint32_t idesc = tc::idesc_bf16(kBM, kBN * ntile);
-          const uint32_t d = tmem + (uint32_t)(kBN * kBGroupTiles * grp);   // onto alpha W
+          const uint32_t d = tmem + (uint32_t)(kBN * i0);
 #pragma unroll
           for (int p = 0; p < np; ++p) {
             const int ao = ((pa[p] >> 1) * kBPcPlane + 64 * (pa[p] & 1)) / 16;
@@ -508,39 +537,6 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
           return;
         }
     };
-    const int cbase = B.cb0 * kBN;
-    // alpha W of tiles [i0, i1) of tensor k from the ring into their tensor-memory homes, then
-    // the group's ready signal (tensor memory written by this warp)
-    auto move = [&](int k, int i0, int i1, int grp, int lr, int half, uint32_t home0) {
-      for (int i = i0; i < i1; ++i) {
-        const int g = k * nt + i, s = g & (kBStages - 1);
-        wait(&sfull[s], (uint32_t)((g / kBStages) & 1));
-        const uint8_t *box = sm + s * kBTile + half * kBBox;
-        uint32_t aw[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 v = *reinterpret_cast<const float4 *>(box + sw(lr, c));
-          aw[4 * c + 0] = __float_as_uint(__fmul_rn(alpha, v.x));
-          aw[4 * c + 1] = __float_as_uint(__fmul_rn(alpha, v.y));
-          aw[4 * c + 2] = __float_as_uint(__fmul_rn(alpha, v.z));
-          aw[4 * c + 3] = __float_as_uint(__fmul_rn(alpha, v.w));
-        }
-        tc::fence_proxy_async_smem();   // the ring slot is refilled by TMA
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sempty[s]);
-        tc::tmem_st16(home0 + (uint32_t)(kBN * i), aw);
-        tc::tmem_st16(home0 + (uint32_t)(kBN * i + 16), aw + 16);
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&hready[grp]);
-    };
-    {
-      const int quarter = warp & 3, half = warp >> 2;
-      move(0, 0, ntile0, 0, quarter * 32 + lane, half, tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half));
-    }
-
     for (int k = 0; k < P.nb; ++k) {
       // the thread's coordinates are re-derived for every tensor from opaque copies, so that
       // the addresses computed from them are not all held live across the batch loop
@@ -555,10 +551,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       const LrEncodeItem &it = P.item[tix(k)];
       const uint32_t kp = (uint32_t)(k & 1);
 
-      // ---------------- alpha W of the second group (the first one moved during the last pack) ----------------
-      if (ngroups == 2) move(k, kBGroupTiles, nt, 1, lr, half, home0);
-
-      // ---------------- W~ amax (and the transformed copy), the next tile's load in flight ----------------
+      // ---------------- W~ = alpha D: amax (and the transformed copy), next tile's load in flight ----------------
       uint32_t m_run = 0;
       uint32_t nxt[32];
       wait(&dfull[0], kp);
@@ -569,7 +562,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
         tc::tmem_wait_ld(nxt);
         uint32_t raw[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) raw[e] = nxt[e];
+        for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(nxt[e])));
         if (i + 1 < nt) {
           if (i + 1 == kBGroupTiles) {
             wait(&dfull[1], kp);
@@ -591,6 +584,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       }
       m_run = warp_max_u32(m_run);
       if (ln == 0) red[wk] = m_run;
+      tc::fence_before_sync();
       tc::named_bar_sync(1, 32 * kBWarps);
       if (EPI == LR_AMAX) {
         // amax only: max-accumulated into the caller's word, no pack
@@ -600,9 +594,13 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
           if (m > 0x7F7FFFFFu) set_status(status, GIFT_ERR_NONFINITE);
           if (m) asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(it.amax_out), "r"(m) : "memory");
         }
+        // every warp's tensor-memory reads are done (the named barrier above)
         tc::fence_before_sync();
         __syncwarp();
-        if (ln == 0) tc::mbar_arrive(&cfree);
+        if (ln == 0) {
+          tc::mbar_arrive(&hfree[0]);
+          if (ngroups == 2) tc::mbar_arrive(&hfree[1]);
+        }
         continue;
       }
       if (tid_k == 0) {
@@ -631,8 +629,9 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
       const ScalePair sp = scale_pair(amax, fmax_of<F>());
       const float s_t = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, kNvfp4TensorDiv);
 
-      // ---------------- pack, one group of four tiles at a time through the Pc region ----------------
-      uint8_t *const stg = sm + kBOffPc;   // free: every MMA of the tensor is done
+      // ---------------- pack, one group of four tiles at a time through the staging region ----------------
+      uint8_t *const stg = sm + kBOffStg;
+      const int cbase = B.cb0 * kBN;
       for (int grp = 0; grp < ngroups; ++grp) {
         const int i0 = kBGroupTiles * grp, i1 = grp == 0 ? ntile0 : nt;
         tc::tmem_ld32_nowait(slot(i0), nxt);
@@ -643,9 +642,16 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
 #pragma unroll
           for (int e = 0; e < 32; ++e) raw[e] = nxt[e];
           if (i + 1 < i1) tc::tmem_ld32_nowait(slot(i + 1), nxt);
+          if (i + 1 == i1) {
+            // this warp's reads of the group are done: the tensor memory takes the next
+            // tensor's W
+            tc::fence_before_sync();
+            __syncwarp();
+            if (ln == 0) tc::mbar_arrive(&hfree[grp]);
+          }
           float v[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[e]);
+          for (int e = 0; e < 32; ++e) v[e] = __fmul_rn(alpha, __uint_as_float(raw[e]));
           if (EPI == LR_PACK_TENSOR) {
             uint32_t w4[8];
 #pragma unroll
@@ -677,11 +683,8 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
             *reinterpret_cast<uint16_t *>(stg + kBOffScales + lr * 16 + 4 * j + 2 * half) = sc;
           }
         }
-        // every worker's tensor-memory reads of the group are done past this barrier (the next
-        // tensor's alpha W goes there), and the group's code rows are complete
-        tc::fence_before_sync();
+        // the group's code rows are complete
         tc::named_bar_sync(1, 32 * kBWarps);
-        tc::fence_after_sync();
         const int gbase = cbase + kBN * i0, ntile = i1 - i0;
         if (EPI == LR_PACK_TENSOR) {
           for (int item = tid_k; item < kBM * 16; item += 32 * kBWarps) {
@@ -706,14 +709,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_lr_apply_batch(const __grid_co
         }
         // the staging is rewritten by the next group
         tc::named_bar_sync(1, 32 * kBWarps);
-        // the first group's homes are packed: the next tensor's first tiles go in while this
-        // tensor's second group is packed
-        if (grp == 0 && k + 1 < P.nb) move(k + 1, 0, ntile0, 0, lr, half, home0);
       }
-      // the region takes the next tensor's Pc planes by TMA
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (ln == 0) tc::mbar_arrive(&cfree);
     }
   }
 

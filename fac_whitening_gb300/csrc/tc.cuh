@@ -133,6 +133,12 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Shared memory -> tensor memory: 128 rows x 32 bytes (the K slice a descriptor selects, in
+// the operand layouts of the MMA descriptors) into lanes 0-127, 8 consecutive 32-bit columns
+// from taddr; asynchronous, in order with this thread's MMAs, tracked by mma_commit.
+__device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;\n" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
