@@ -387,18 +387,23 @@ def main_gift(args):
                   lambda it, w: G.gift_decode(ctx, it[0], it[1]["avg"], False, "f32", "tensor", d_out, d_in,
                                               it[1]["out"], ws=w, status=st))
 
+    def euclid_amax(E, w):
+        # the shared amax of the tensor's R replicas (one streaming launch)
+        G.gift_amax_replicas(ctx, None, E["W"], FMT, "tensor", E["shared"], ws=w, status=st)
+
+    def euclid_encode(E, w):
+        # replicas in reverse order of their amax pass: the most recently read ones are still
+        # in L2 when their pack pass runs
+        rev = list(reversed(range(R)))
+        G.gift_encode_replicas(ctx, None, [E["W"][r] for r in rev], FMT, "tensor", [E["codes"][r] for r in rev],
+                               scales=[E["scales"][r] for r in rev], amax_in=[E["shared"]] * R, ws=w, status=st)
+
     def e_amax():
         shared.zero_()
-        fork_join([(E, r) for E in eu for r in range(R)],
-                  lambda it, w: G.gift_amax(ctx, None, it[0]["W"][it[1]], FMT, "tensor", it[0]["shared"], ws=w,
-                                            status=st))
+        fork_join(eu, euclid_amax)
 
     def e_encode():
-        # replicas in reverse order of their amax pass: the most recently read ones are
-        # still in L2 when their pack pass runs
-        fork_join([(E, r) for E in eu for r in reversed(range(R))],
-                  lambda it, w: G.gift_encode(ctx, None, it[0]["W"][it[1]], FMT, "tensor", it[0]["codes"][it[1]],
-                                              it[0]["scales"][it[1]], amax_in=it[0]["shared"], ws=w, status=st))
+        fork_join(eu, euclid_encode)
 
     def e_reduce():
         fork_join(eu, lambda E, w: G.gift_replica_reduce(ctx, E["codes"], E["scales"], FMT, "tensor",
@@ -412,8 +417,8 @@ def main_gift(args):
     alg = {"gift_encode": (R * n_gift * 5, len(gl), len(gl)),
            "gift_reduce": (n_gift * (R + 4), len(gl), len(gl)),
            "gift_decode": (n_gift * 8, len(gl) * 3, len(gl)),
-           "euclid_amax": (R * n_eu * 4, len(eu) * R, len(eu) * R),
-           "euclid_encode": (R * n_eu * 5, len(eu) * R, len(eu) * R),
+           "euclid_amax": (R * n_eu * 4, len(eu), len(eu)),
+           "euclid_encode": (R * n_eu * 5, len(eu), len(eu)),
            "euclid_reduce": (n_eu * (R + 4), len(eu), len(eu))}
     kernels_per_step = sum(v[1] for v in alg.values())
     grad_bytes = R * 4 * (n_gift + n_eu)
@@ -509,11 +514,8 @@ def main_gift(args):
                 G.gift_decode(ctx, f, X["avg"], False, "f32", "tensor", d_out, d_in, X["out"], ws=w, status=st)
             else:
                 X["shared"].zero_()
-                for r in range(R):
-                    G.gift_amax(ctx, None, X["W"][r], FMT, "tensor", X["shared"], ws=w, status=st)
-                for r in reversed(range(R)):
-                    G.gift_encode(ctx, None, X["W"][r], FMT, "tensor", X["codes"][r], X["scales"][r],
-                                  amax_in=X["shared"], ws=w, status=st)
+                euclid_amax(X, w)
+                euclid_encode(X, w)
                 G.gift_replica_reduce(ctx, X["codes"], X["scales"], FMT, "tensor", X["spec"].d_out,
                                       X["spec"].d_in, X["avg"], status=st)
 

@@ -692,10 +692,85 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
     gift_status st = GIFT_OK;
     if (try_batch(ctx, f, d_out, d_in, fmt, prec, w, L, R, items, &st)) return st;
   }
+  if (kind == GIFT_XF_IDENTITY && (fmt == GIFT_FMT_E4M3 || fmt == GIFT_FMT_E5M2) && scaling == GIFT_SCALE_TENSOR) {
+    // one streaming launch for the replicas' own amax (those without a caller amax), one for
+    // the pack
+    const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
+    const size_t n = (size_t)d_out * d_in;
+    MultiArgs m;
+    std::memset(&m, 0, sizeof(m));
+    MultiArgs own;
+    std::memset(&own, 0, sizeof(own));
+    int nown = 0;
+    for (int r = 0; r < R; ++r) {
+      m.x[r] = W[r];
+      m.codes[r] = static_cast<uint8_t *>(codes[r]);
+      m.scale[r] = static_cast<float *>(scales[r]);
+      m.amax_out[r] = at(amax_out, r);
+      m.amax_in[r] = at(amax_in, r);
+      if (!m.amax_in[r]) {
+        m.amax_in[r] = w.amax + r;   // the workspace holds 64 amax words
+        own.x[nown] = W[r];
+        own.amax_bits[nown++] = reinterpret_cast<uint32_t *>(w.amax + r);
+      }
+    }
+    if (multi_ok(m, R, n, true)) {
+      if (nown) {
+        CK(cudaMemsetAsync(w.amax, 0, (size_t)R * sizeof(float), stream));
+        CK(launch_amax_multi(L, own, nown, n));
+      }
+      CK(launch_pack_tensor_multi(L, fmt, m, R, n));
+      return GIFT_OK;
+    }
+  }
   for (int r = 0; r < R; ++r) {
     const gift_status st = gift_encode(ctx, f, W[r], d_out, d_in, fmt, scaling, prec, at(amax_in, r), nullptr,
                                        codes[r], at(scales, r), at(tensor_scales, r), nullptr, at(amax_out, r), ws,
                                        ws_bytes, d_status, stream);
+    if (st != GIFT_OK) return st;
+  }
+  return GIFT_OK;
+}
+
+gift_status gift_amax_replicas(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W, int d_out,
+                               int d_in, gift_format fmt, gift_scaling scaling, gift_precision prec,
+                               float *amax_accum, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  if (!ctx || !W || !amax_accum || R < 1 || R > kMaxReplicas || fmt == GIFT_FMT_F32) return GIFT_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r) {
+    const gift_status cs = codec_common_checks(ctx, f, W[r], d_out, d_in, fmt, scaling);
+    if (cs != GIFT_OK) return cs;
+  }
+  const gift_xform kind = kind_of(f);
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const Launch L = mk(ctx, d_status, stream);
+  const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
+  if (!block && kind == GIFT_XF_IDENTITY) {
+    MultiArgs m;
+    std::memset(&m, 0, sizeof(m));
+    for (int r = 0; r < R; ++r) {
+      m.x[r] = W[r];
+      m.amax_bits[r] = reinterpret_cast<uint32_t *>(amax_accum);
+    }
+    if (multi_ok(m, R, (size_t)d_out * d_in, false)) {
+      CK(launch_amax_multi(L, m, R, (size_t)d_out * d_in));
+      return GIFT_OK;
+    }
+  }
+  if (!block && kind == GIFT_XF_LOWRANK) {
+    const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
+    LrEncodeItem items[kMaxReplicas];
+    std::memset(items, 0, sizeof(items));
+    for (int r = 0; r < R; ++r) {
+      items[r].X = W[r];
+      items[r].amax_out = amax_accum;   // max-accumulated by every replica
+    }
+    gift_status st = GIFT_OK;
+    if (try_batch(ctx, f, d_out, d_in, fmt, prec, w, L, R, items, &st, true)) return st;
+  }
+  for (int r = 0; r < R; ++r) {
+    const gift_status st = gift_amax(ctx, f, W[r], d_out, d_in, fmt, scaling, prec, nullptr, amax_accum, ws,
+                                     ws_bytes, d_status, stream);
     if (st != GIFT_OK) return st;
   }
   return GIFT_OK;

@@ -24,6 +24,16 @@ struct ReduceArgs {
   const float *tscales[kMaxReplicas];
 };
 
+// Several tensors of one size in one streaming launch (quant.cu).
+struct MultiArgs {
+  const float *x[kMaxReplicas];
+  uint8_t *codes[kMaxReplicas];        // pack: E4M3 / E5M2 codes of each tensor
+  float *scale[kMaxReplicas];          // pack: each tensor's scale s
+  const float *amax_in[kMaxReplicas];  // pack: the amax each tensor is scaled with
+  float *amax_out[kMaxReplicas];       // pack: nullable copies of it
+  uint32_t *amax_bits[kMaxReplicas];   // amax: max-accumulated |x| bit pattern of each tensor
+};
+
 // ---- quant.cu ---------------------------------------------------------------------------
 cudaError_t launch_amax(const Launch &L, const float *x, const float *r, size_t n, float *amax_accum);
 cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *r, size_t n, const float *amax,
@@ -39,6 +49,10 @@ cudaError_t launch_hits_tensor(const Launch &L, int fmt, const float *x, size_t 
                                unsigned long long *counts);
 cudaError_t launch_reduce(const Launch &L, const ReduceArgs &a, int R, int fmt, int scaling, int d_out, int d_in,
                           float *out);
+// 16-byte aligned tensors, n a multiple of 4 (and 4-byte aligned codes for the pack).
+bool multi_ok(const MultiArgs &a, int R, size_t n, bool pack);
+cudaError_t launch_amax_multi(const Launch &L, const MultiArgs &a, int R, size_t n);
+cudaError_t launch_pack_tensor_multi(const Launch &L, int fmt, const MultiArgs &a, int R, size_t n);
 
 // ---- lowrank.cu -------------------------------------------------------------------------
 // Split-K projection P = X U (d_out x 32, zero-padded beyond rank); partials to `part`.

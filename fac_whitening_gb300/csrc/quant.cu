@@ -108,6 +108,68 @@ __global__ void __launch_bounds__(256) k_pack_tensor(const float *__restrict__ x
 }
 
 // =====================================================================================
+// The same amax and pack over several tensors of one size in one launch (the replicas of a
+// layer): the CTAs walk the tensors in order, each thread with four 16-byte loads in flight.
+// Per element the arithmetic is that of k_amax / k_pack_tensor.
+// =====================================================================================
+__global__ void __launch_bounds__(256) k_amax_multi(MultiArgs a, int R, size_t n4, int *status) {
+  __shared__ uint32_t red[8];
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (int t = 0; t < R; ++t) {
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.x[t]);
+    uint32_t m = 0;
+    size_t i = tid;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = x4[i + u * stride];   // kept in L2 for the pack pass
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m = max(m, max(max(abs_bits(v[u].x), abs_bits(v[u].y)), max(abs_bits(v[u].z), abs_bits(v[u].w))));
+    }
+    for (; i < n4; i += stride) {
+      const float4 v = x4[i];
+      m = max(m, max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w))));
+    }
+    m = block_max_u32<256>(m, red);
+    if (threadIdx.x == 0) {
+      if (m) atomicMax(a.amax_bits[t], m);
+      if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+    }
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(256) k_pack_tensor_multi(MultiArgs a, int R, size_t n4, int *status) {
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (int t = 0; t < R; ++t) {
+    const float amax = *a.amax_in[t];
+    const ScalePair sp = scale_pair(amax, fmax_of<F>());
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (!(amax <= kF32Max)) set_status(status, GIFT_ERR_NONFINITE);
+      a.scale[t][0] = sp.s;
+      if (a.amax_out[t]) a.amax_out[t][0] = amax;
+    }
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.x[t]);
+    uint32_t *c4 = reinterpret_cast<uint32_t *>(a.codes[t]);
+    auto code = [&](const float4 &v) {
+      return pack4_fp8<F>(__fmul_rn(v.x, sp.m), __fmul_rn(v.y, sp.m), __fmul_rn(v.z, sp.m), __fmul_rn(v.w, sp.m));
+    };
+    size_t i = tid;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) c4[i + u * stride] = code(v[u]);
+    }
+    for (; i < n4; i += stride) c4[i] = code(__ldcs(x4 + i));
+  }
+}
+
+// =====================================================================================
 // FP32 "format": codes are the values themselves (lossless path); residual becomes 0.
 // =====================================================================================
 template <bool RES, bool TOUT>
@@ -528,6 +590,12 @@ static int stream_grid(const Launch &L, size_t work, int per_cta) {
 }
 
 cudaError_t launch_amax(const Launch &L, const float *x, const float *r, size_t n, float *amax_accum) {
+  if (!r && aligned16(x) && n % 4 == 0) {   // the streaming multi-tensor kernel, one tensor
+    MultiArgs m;
+    m.x[0] = x;
+    m.amax_bits[0] = reinterpret_cast<uint32_t *>(amax_accum);
+    return launch_amax_multi(L, m, 1, n);
+  }
   const bool vec = aligned16(x) && (r == nullptr || aligned16(r));
   const int grid = stream_grid(L, (n + 3) / 4, 256);
   uint32_t *ab = reinterpret_cast<uint32_t *>(amax_accum);
@@ -552,6 +620,15 @@ static void pack_tensor_dispatch(const Launch &L, int grid, const float *x, floa
 
 cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *r, size_t n, const float *amax,
                                uint8_t *codes, float *scale, float *amax_out, float *tout) {
+  if (!r && !tout && aligned16(x) && n % 4 == 0 && ((uintptr_t)codes & 3u) == 0) {   // one tensor, streaming
+    MultiArgs m;
+    m.x[0] = x;
+    m.codes[0] = codes;
+    m.scale[0] = scale;
+    m.amax_in[0] = amax;
+    m.amax_out[0] = amax_out;
+    return launch_pack_tensor_multi(L, fmt, m, 1, n);
+  }
   const bool vec = aligned16(x) && (!r || aligned16(r)) && (!tout || aligned16(tout)) &&
                    (((uintptr_t)codes & 3u) == 0);
   const int grid = stream_grid(L, (n + 3) / 4, 256);
@@ -562,6 +639,28 @@ cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *
     if (vec) pack_tensor_dispatch<FMT_E5M2, true>(L, grid, x, r, n, amax, codes, scale, amax_out, tout);
     else pack_tensor_dispatch<FMT_E5M2, false>(L, grid, x, r, n, amax, codes, scale, amax_out, tout);
   }
+  return cudaGetLastError();
+}
+
+bool multi_ok(const MultiArgs &a, int R, size_t n, bool pack) {
+  if (R < 1 || R > kMaxReplicas || n % 4) return false;
+  for (int t = 0; t < R; ++t) {
+    if (!aligned16(a.x[t])) return false;
+    if (pack && ((uintptr_t)a.codes[t] & 3u)) return false;
+  }
+  return true;
+}
+
+cudaError_t launch_amax_multi(const Launch &L, const MultiArgs &a, int R, size_t n) {
+  const int grid = stream_grid(L, n / 4, 1024);
+  k_amax_multi<<<grid, 256, 0, L.stream>>>(a, R, n / 4, L.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_tensor_multi(const Launch &L, int fmt, const MultiArgs &a, int R, size_t n) {
+  const int grid = stream_grid(L, n / 4, 1024);
+  if (fmt == GIFT_FMT_E4M3) k_pack_tensor_multi<FMT_E4M3><<<grid, 256, 0, L.stream>>>(a, R, n / 4, L.status);
+  else k_pack_tensor_multi<FMT_E5M2><<<grid, 256, 0, L.stream>>>(a, R, n / 4, L.status);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,8 @@ def _declare(lib):
         "gift_encode_replicas": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), _i, _i, _i, _i, _i,
                                       ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                       ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _sz, _vp, _vp]),
+        "gift_amax_replicas": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _vp,
+                                    _vp, _sz, _vp, _vp]),
         "gift_replica_reduce": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i, _i,
                                      _i, _i, _vp, _vp, _vp]),
         "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
@@ -276,6 +278,16 @@ def gift_encode_replicas(ctx: Context, f: Optional[Factor], Ws: Sequence, fmt: s
                                       PREC[prec], arr(amax_in), arr(codes), arr(scales), arr(tensor_scales),
                                       arr(amax_out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                       _p(status), _stream(stream)), "gift_encode_replicas")
+
+
+def gift_amax_replicas(ctx: Context, f: Optional[Factor], Ws: Sequence, fmt: str, scaling: str, amax_accum,
+                       prec: str = "fp32", ws=None, status=None, stream=None):
+    R = len(Ws)
+    d_out, d_in = Ws[0].shape
+    _check(lib().gift_amax_replicas(ctx.handle, _fptr(f), R, (_vp * R)(*[_p(W) for W in Ws]), d_out, d_in, FMT[fmt],
+                                    SCALING[scaling], PREC[prec], _p(amax_accum), _p(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                    _stream(stream)), "gift_amax_replicas")
 
 
 def gift_replica_reduce(ctx: Context, codes: Sequence, scales: Optional[Sequence], fmt: str, scaling: str,

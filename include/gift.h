@@ -273,6 +273,17 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
                                  float *const *tensor_scales, float *const *amax_out, void *ws,
                                  size_t ws_bytes, int *d_status, cudaStream_t stream);
 
+/* The shared amax of R replicas (the AllReduceMax of the scale in [notes] Algorithm 1, for R
+ * workers modelled on one GPU): max-accumulates into amax_accum the amax that gift_amax would
+ * give for each of the R tensors W[r] (host array of R device pointers, 1 <= R <= 64).  Same
+ * result as R gift_amax calls without residual; identity and rank-r factors with per-tensor
+ * scaling take one streaming pass over all replicas.  ws: gift_workspace_bytes(GIFT_OP_AMAX,
+ * ...).  d_status: NONFINITE. */
+gift_status gift_amax_replicas(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W,
+                               int d_out, int d_in, gift_format fmt, gift_scaling scaling,
+                               gift_precision prec, float *amax_accum, void *ws, size_t ws_bytes,
+                               int *d_status, cudaStream_t stream);
+
 /* Replica reduce: out = (sum_r deq_r) / R in FP32, adding replicas in order r = 0..R-1
  * with each replica dequantised with its own scale ([notes] eq. (1) data-parallel average;
  * Algorithm 1 AllReduceSum, Dequantize, divide by N — modelled on one GPU over R code

@@ -145,3 +145,33 @@ def test_encode_replicas_rejects_before_enqueueing():
         G.gift_encode_replicas(ctx(), f, Ws, "e4m3", "tensor", [codes[0], Ws[1], codes[2]], scales=scales, ws=w)
     torch.cuda.synchronize()
     assert all(int((c != 0xA5).sum()) == 0 for c in codes)
+
+
+@pytest.mark.parametrize("kind,shape", [("identity", (1536, 1536)), ("identity", (1000, 2048)),
+                                        ("lowrank", (1536, 6144))])
+def test_amax_replicas_matches_single_calls(kind, shape):
+    # the shared amax of R replicas (one streaming pass) equals the max of R gift_amax calls
+    fac = rand_factor(*shape, seed=16)
+    f = None if kind == "identity" else fac
+    Ws = replicas(fac, 5, seed=26)
+    w = ws("amax", kind, "e4m3", "tensor", *shape)
+    acc = torch.zeros(1, device=DEV)
+    G.gift_amax_replicas(ctx(), f, Ws, "e4m3", "tensor", acc, ws=w)
+    one = torch.zeros(1, device=DEV)
+    for W in Ws:
+        G.gift_amax(ctx(), f, W, "e4m3", "tensor", one, ws=w)
+    torch.cuda.synchronize()
+    assert acc.item() == one.item() > 0
+
+
+def test_encode_replicas_identity_shared_amax():
+    # the Euclidean path with a shared scale: one pack launch for all replicas
+    fac = rand_factor(1536, 1536, seed=17)
+    Ws = replicas(fac, 6, seed=27)
+    shared = torch.zeros(1, device=DEV)
+    G.gift_amax_replicas(ctx(), None, Ws, "e5m2", "tensor", shared, ws=ws("amax", "identity", "e5m2", "tensor", 1536, 1536))
+    torch.cuda.synchronize()
+    a = run_batched(None, Ws, "e5m2", "tensor", "fp32", amax_in=[shared] * 6)
+    b = run_single(None, Ws, "e5m2", "tensor", "fp32", amax_in=[shared] * 6)
+    assert_same(a, b)
+    assert all(o["amax"].item() == shared.item() for o in a[0])
