@@ -477,18 +477,30 @@ __global__ void __launch_bounds__(256) k_reduce_fp8_vec(ReduceArgs a, int R, siz
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
     float acc[16];
     const size_t e0 = i << 4;
-    for (int rr = 0; rr < R; ++rr) {
-      const uint4 c = reinterpret_cast<const uint4 *>(a.codes[rr])[i];
-      const float s = replica_scale<BLOCK>(a, rr, e0, d_in, nbc);
-      const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    // the replicas' code chunks are loaded 8 at a time (8 loads in flight per thread), then
+    // added in replica order
+    for (int r0 = 0; r0 < R; r0 += 8) {
+      uint4 cc[8];
+      float sc[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float d = __fmul_rn(dec_fp8<F>((w[q] >> (8 * b)) & 0xFFu), s);
-          acc[4 * q + b] = (rr == 0) ? d : __fadd_rn(acc[4 * q + b], d);
+      for (int u = 0; u < 8; ++u)
+        if (r0 + u < R) {
+          cc[u] = __ldcs(reinterpret_cast<const uint4 *>(a.codes[r0 + u]) + i);
+          sc[u] = replica_scale<BLOCK>(a, r0 + u, e0, d_in, nbc);
         }
-      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (r0 + u < R) {
+          const uint32_t w[4] = {cc[u].x, cc[u].y, cc[u].z, cc[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const float d = __fmul_rn(dec_fp8<F>((w[q] >> (8 * b)) & 0xFFu), sc[u]);
+              acc[4 * q + b] = (r0 + u == 0) ? d : __fadd_rn(acc[4 * q + b], d);
+            }
+          }
+        }
     }
     float4 *o = reinterpret_cast<float4 *>(out + e0);
 #pragma unroll
