@@ -414,9 +414,11 @@ def main_gift(args):
     n_gift = len(gl) * d_out * d_in
     n_eu = sum(E["spec"].d_out * E["spec"].d_in for E in eu)
     # algorithmic bytes and launches of each group (per step)
-    alg = {"gift_encode": (R * n_gift * 5, len(gl), len(gl)),
+    # (gift_encode_replicas: projection pass, Pc reduce, apply-and-pack pass; the decode of a
+    # factor with cached planes: tensor-core projection and the pipelined apply)
+    alg = {"gift_encode": (R * n_gift * 5, len(gl) * 3, len(gl)),
            "gift_reduce": (n_gift * (R + 4), len(gl), len(gl)),
-           "gift_decode": (n_gift * 8, len(gl) * 3, len(gl)),
+           "gift_decode": (n_gift * 8, len(gl) * 2, len(gl)),
            "euclid_amax": (R * n_eu * 4, len(eu), len(eu)),
            "euclid_encode": (R * n_eu * 5, len(eu), len(eu)),
            "euclid_reduce": (n_eu * (R + 4), len(eu), len(eu))}
@@ -555,6 +557,31 @@ def main_gift(args):
         torch.distributed.destroy_process_group()
 
 
+def near_gpu_cpus(device):
+    """The CPU cores the platform lists as local to the GPU (sysfs, by its PCI address), or
+    None.  Pinned host buffers allocated and first touched by a thread on those cores sit on
+    the GPU's own memory node."""
+    import torch
+    p = torch.cuda.get_device_properties(device)
+    dom, bus, dv = (getattr(p, "pci_domain_id", None), getattr(p, "pci_bus_id", None),
+                    getattr(p, "pci_device_id", None))
+    if bus is None or dom is None or dv is None:
+        return None
+    path = f"/sys/bus/pci/devices/{dom:04x}:{bus:02x}:{dv:02x}.0/local_cpulist"
+    try:
+        text = open(path).read().strip()
+    except OSError:
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return sorted(cpus & os.sched_getaffinity(0)) or None
+
+
 def run_e2e(args, gl, eu, dev, grad_bytes, world, item_ops):
     """Same step through the public API with host buffers.  Per step, every replica gradient
     is copied from pinned host memory and every decoded / averaged result is read back to
@@ -563,6 +590,9 @@ def run_e2e(args, gl, eu, dev, grad_bytes, world, item_ops):
     inputs have landed, and a read-back stream downloads each result as soon as it exists.
     Every rank does this; the slowest rank's time counts."""
     import torch
+    cpus = near_gpu_cpus(dev)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
     items = [("gift", i, L) for i, L in enumerate(gl)] + [("euclid", j, E) for j, E in enumerate(eu)]
     host_in = [[torch.empty(W.shape, dtype=torch.float32, pin_memory=True) for W in it[2]["W"]] for it in items]
     for hs, it in zip(host_in, items):
@@ -615,7 +645,8 @@ def run_e2e(args, gl, eu, dev, grad_bytes, world, item_ops):
     ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / steps
     return {"value": job_value(world, grad_bytes, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
-            "pipeline": "per-tensor upload, codec and read-back on three streams"}
+            "pipeline": "per-tensor upload, codec and read-back on three streams",
+            "host_cpus": f"{len(cpus)} cores local to the GPU" if cpus else "not pinned (no locality information)"}
 
 
 def main():
