@@ -6,14 +6,15 @@ geometry-aware branch (rank-32 input-side whitening, E4M3 per-tensor local scale
 and 60 Euclidean tensors (1536 x 1536 / 1536 x 6144) take the Euclidean path
 (AllReduceMax'd shared scale), each over R = 8 replica gradients held in HBM:
   geometry-aware layer: 8 x gift_encode -> gift_replica_reduce -> gift_decode
-  Euclidean tensor:     8 x gift_amax   -> 8 x gift_encode(shared amax) -> gift_replica_reduce
+  Euclidean tensor:     8 x (amax -> shared amax -> gift_encode with it) -> gift_replica_reduce
+                        (the first two steps are one gift_encode_replicas_shared call)
 The factor refresh (gift_factor_update on each layer's activations, T = 16384 BF16)
 runs every K = 50 steps in the method and is timed separately.
 
 value = FP32 gradient bytes entering the codec per step (sum over tensors of
 R * 4 * d_out * d_in) / step time, in GB/s, device-resident inputs, inputs larger
 than L2 (so no flush is needed).  Each stage group is captured in its own CUDA graph;
-a step replays the six graphs on one stream and CUDA events between them give each
+a step replays the five graphs on one stream and CUDA events between them give each
 group's time inside the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gift|reference]
@@ -99,8 +100,7 @@ def solo_call_ms(graph, calls, reps):
 
 # stage group -> (ncu summary under profiles/, the kernel source its counters belong to)
 PROFILES = {"gift_encode": ("encode_batch_1536x6144.md", "lowrank_batch.cu"),
-            "euclid_encode": ("pack_tensor_600m_shapes.md", "quant.cu"),
-            "euclid_amax": ("pack_tensor_600m_shapes.md", "quant.cu")}
+            "euclid_encode": ("encode_shared_600m_shapes.md", "quant.cu")}
 
 
 def profiled_traffic(group):
@@ -387,20 +387,10 @@ def main_gift(args):
                   lambda it, w: G.gift_decode(ctx, it[0], it[1]["avg"], False, "f32", "tensor", d_out, d_in,
                                               it[1]["out"], ws=w, status=st))
 
-    def euclid_amax(E, w):
-        # the shared amax of the tensor's R replicas (one streaming launch)
-        G.gift_amax_replicas(ctx, None, E["W"], FMT, "tensor", E["shared"], ws=w, status=st)
-
     def euclid_encode(E, w):
-        # replicas in reverse order of their amax pass: the most recently read ones are still
-        # in L2 when their pack pass runs
-        rev = list(reversed(range(R)))
-        G.gift_encode_replicas(ctx, None, [E["W"][r] for r in rev], FMT, "tensor", [E["codes"][r] for r in rev],
-                               scales=[E["scales"][r] for r in rev], amax_in=[E["shared"]] * R, ws=w, status=st)
-
-    def e_amax():
-        shared.zero_()
-        fork_join(eu, euclid_amax)
+        # the R replicas' shared amax and their pack with it: one cooperative launch
+        G.gift_encode_replicas_shared(ctx, None, E["W"], FMT, "tensor", E["codes"], E["scales"],
+                                      shared_amax_out=E["shared"], ws=w, status=st)
 
     def e_encode():
         fork_join(eu, euclid_encode)
@@ -410,7 +400,7 @@ def main_gift(args):
                                                          E["spec"].d_out, E["spec"].d_in, E["avg"], status=st))
 
     groups = [("gift_encode", g_encode), ("gift_reduce", g_reduce), ("gift_decode", g_decode),
-              ("euclid_amax", e_amax), ("euclid_encode", e_encode), ("euclid_reduce", e_reduce)]
+              ("euclid_encode", e_encode), ("euclid_reduce", e_reduce)]
     n_gift = len(gl) * d_out * d_in
     n_eu = sum(E["spec"].d_out * E["spec"].d_in for E in eu)
     # algorithmic bytes and launches of each group (per step)
@@ -419,7 +409,6 @@ def main_gift(args):
     alg = {"gift_encode": (R * n_gift * 5, len(gl) * 3, len(gl)),
            "gift_reduce": (n_gift * (R + 4), len(gl), len(gl)),
            "gift_decode": (n_gift * 8, len(gl) * 2, len(gl)),
-           "euclid_amax": (R * n_eu * 4, len(eu), len(eu)),
            "euclid_encode": (R * n_eu * 5, len(eu), len(eu)),
            "euclid_reduce": (n_eu * (R + 4), len(eu), len(eu))}
     kernels_per_step = sum(v[1] for v in alg.values())
@@ -482,9 +471,10 @@ def main_gift(args):
     value = job_value(world, grad_bytes, ms)
 
     # ---- roofline of the dominant kernel ----------------------------------------------
-    # The dominant group is normally the rank-r encode: one gift_encode_replicas call per
-    # layer encodes its R replicas (projection pass, Pc reduce, apply-and-pack pass).  Its
-    # call duration is timed on its own: the group's calls replayed back to back on one
+    # The dominant group is the Euclidean shared-scale encode (one cooperative launch per
+    # tensor: amax of its R replicas, grid barrier, pack) or the rank-r encode (one
+    # gift_encode_replicas call per layer: projection pass, Pc reduce, apply-and-pack pass).
+    # Its call duration is timed on its own: the group's calls replayed back to back on one
     # stream (CUDA events around the replays), so calls do not overlap.
     dom = max(group_ms, key=group_ms.get)
     bytes_g, launches_g, calls_g = alg[dom]
@@ -515,8 +505,6 @@ def main_gift(args):
                 G.gift_replica_reduce(ctx, X["codes"], X["scales"], FMT, "tensor", d_out, d_in, X["avg"], status=st)
                 G.gift_decode(ctx, f, X["avg"], False, "f32", "tensor", d_out, d_in, X["out"], ws=w, status=st)
             else:
-                X["shared"].zero_()
-                euclid_amax(X, w)
                 euclid_encode(X, w)
                 G.gift_replica_reduce(ctx, X["codes"], X["scales"], FMT, "tensor", X["spec"].d_out,
                                       X["spec"].d_in, X["avg"], status=st)

@@ -732,6 +732,57 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
   return GIFT_OK;
 }
 
+// Two workspace amax words beyond those of the batched rank-r encode and of the replicas'
+// own amax: the shared amax and the barrier count of the shared-scale encode.
+constexpr int kSharedAmaxWord = 62;
+
+gift_status gift_encode_replicas_shared(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W,
+                                        int d_out, int d_in, gift_format fmt, gift_scaling scaling,
+                                        gift_precision prec, void *const *codes, void *const *scales,
+                                        float *const *tensor_scales, float *shared_amax_out, void *ws,
+                                        size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  if (!ctx || !W || !codes || !scales || R < 1 || R > kMaxReplicas) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_F32) return GIFT_ERR_INVALID_ARG;   // no scale to share
+  if (fmt != GIFT_FMT_NVFP4 && scaling != GIFT_SCALE_TENSOR) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && !tensor_scales) return GIFT_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r) {
+    const gift_status cs = encode_checks(ctx, f, W[r], d_out, d_in, fmt, scaling, nullptr, codes[r], scales[r],
+                                         tensor_scales ? tensor_scales[r] : nullptr, ws, ws_bytes);
+    if (cs != GIFT_OK) return cs;
+  }
+  const gift_xform kind = kind_of(f);
+  const Launch L = mk(ctx, d_status, stream);
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
+  float *word = w.amax + kSharedAmaxWord;
+  const size_t n = (size_t)d_out * d_in;
+  if (kind == GIFT_XF_IDENTITY && fmt != GIFT_FMT_NVFP4) {
+    MultiArgs m;
+    std::memset(&m, 0, sizeof(m));
+    for (int r = 0; r < R; ++r) {
+      m.x[r] = W[r];
+      m.codes[r] = static_cast<uint8_t *>(codes[r]);
+      m.scale[r] = static_cast<float *>(scales[r]);
+    }
+    if (multi_ok(m, R, n, true)) {
+      CK(cudaMemsetAsync(word, 0, 2 * sizeof(float), stream));   // amax bits, barrier count
+      CK(launch_encode_shared(L, fmt, m, R, n, reinterpret_cast<uint32_t *>(word), shared_amax_out));
+      return GIFT_OK;
+    }
+  }
+  // any other kind, format or layout: the shared amax, then every replica encoded with it
+  CK(cudaMemsetAsync(word, 0, sizeof(float), stream));
+  gift_status st = gift_amax_replicas(ctx, f, R, W, d_out, d_in, fmt, scaling, prec, word, ws, ws_bytes, d_status,
+                                      stream);
+  if (st != GIFT_OK) return st;
+  const float *ain[kMaxReplicas];
+  for (int r = 0; r < R; ++r) ain[r] = word;
+  st = gift_encode_replicas(ctx, f, R, W, d_out, d_in, fmt, scaling, prec, ain, codes, scales, tensor_scales,
+                            nullptr, ws, ws_bytes, d_status, stream);
+  if (st != GIFT_OK) return st;
+  if (shared_amax_out) CK(cudaMemcpyAsync(shared_amax_out, word, sizeof(float), cudaMemcpyDeviceToDevice, stream));
+  return GIFT_OK;
+}
+
 gift_status gift_amax_replicas(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W, int d_out,
                                int d_in, gift_format fmt, gift_scaling scaling, gift_precision prec,
                                float *amax_accum, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {

@@ -53,6 +53,10 @@ cudaError_t launch_reduce(const Launch &L, const ReduceArgs &a, int R, int fmt, 
 bool multi_ok(const MultiArgs &a, int R, size_t n, bool pack);
 cudaError_t launch_amax_multi(const Launch &L, const MultiArgs &a, int R, size_t n);
 cudaError_t launch_pack_tensor_multi(const Launch &L, int fmt, const MultiArgs &a, int R, size_t n);
+// the R tensors of a (x, codes, scale, amax_out) packed with the max of their amax (cooperative
+// launch); ws: two words, zero before the launch; shared_out nullable
+cudaError_t launch_encode_shared(const Launch &L, int fmt, const MultiArgs &a, int R, size_t n, uint32_t *ws,
+                                 float *shared_out);
 
 // ---- lowrank.cu -------------------------------------------------------------------------
 // Split-K projection P = X U (d_out x 32, zero-padded beyond rank); partials to `part`.

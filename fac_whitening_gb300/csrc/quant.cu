@@ -9,7 +9,11 @@
 // GIFT abstract (shd-paper.top): NVFP4 as the second low-precision format.
 //
 // Every kernel is HBM-bound: 16-byte loads and stores, grid-stride loops sized to the SM
-// count, warp-shuffle reductions and one atomic per CTA (or warp).
+// count, warp-shuffle reductions and one atomic per CTA (or warp).  The shared-scale encode of
+// several replicas is one cooperative launch with one grid-wide barrier between its amax and
+// pack passes.
+#include <cstring>
+
 #include "kernels.cuh"
 
 namespace gift {
@@ -112,26 +116,98 @@ __global__ void __launch_bounds__(256) k_pack_tensor(const float *__restrict__ x
 // layer): the CTAs walk the tensors in order, each thread with four 16-byte loads in flight.
 // Per element the arithmetic is that of k_amax / k_pack_tensor.
 // =====================================================================================
+// max |x| bit pattern over the thread's grid-stride share of n4 float4s
+__device__ __forceinline__ uint32_t amax_pass(const float4 *__restrict__ x4, size_t n4, size_t tid, size_t stride) {
+  uint32_t m = 0;
+  size_t i = tid;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = x4[i + u * stride];   // kept in L2 for the pack pass
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      m = max(m, max(max(abs_bits(v[u].x), abs_bits(v[u].y)), max(abs_bits(v[u].z), abs_bits(v[u].w))));
+  }
+  for (; i < n4; i += stride) {
+    const float4 v = x4[i];
+    m = max(m, max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w))));
+  }
+  return m;
+}
+
+// codes of the thread's grid-stride share of n4 float4s with multiplier sp.m; inputs and codes
+// are marked evict-first in L2 (neither is read again by this launch)
+template <int F>
+__device__ __forceinline__ void pack_pass(const float4 *__restrict__ x4, uint32_t *__restrict__ c4, size_t n4,
+                                          size_t tid, size_t stride, const ScalePair sp) {
+  auto code = [&](const float4 &v) {
+    return pack4_fp8<F>(__fmul_rn(v.x, sp.m), __fmul_rn(v.y, sp.m), __fmul_rn(v.z, sp.m), __fmul_rn(v.w, sp.m));
+  };
+  size_t i = tid;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) __stcs(c4 + i + u * stride, code(v[u]));
+  }
+  for (; i < n4; i += stride) __stcs(c4 + i, code(__ldcs(x4 + i)));
+}
+
+// the same two passes over two tensors at once (eight 16-byte loads in flight per thread)
+__device__ __forceinline__ uint32_t amax_pass2(const float4 *__restrict__ xa, const float4 *__restrict__ xb, size_t n4,
+                                               size_t tid, size_t stride) {
+  uint32_t m = 0;
+  size_t i = tid;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = xa[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[4 + u] = xb[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      m = max(m, max(max(abs_bits(v[u].x), abs_bits(v[u].y)), max(abs_bits(v[u].z), abs_bits(v[u].w))));
+  }
+  for (; i < n4; i += stride) {
+    const float4 v = xa[i], w = xb[i];
+    m = max(m, max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w))));
+    m = max(m, max(max(abs_bits(w.x), abs_bits(w.y)), max(abs_bits(w.z), abs_bits(w.w))));
+  }
+  return m;
+}
+
+template <int F>
+__device__ __forceinline__ void pack_pass2(const float4 *__restrict__ xa, uint32_t *__restrict__ ca,
+                                           const float4 *__restrict__ xb, uint32_t *__restrict__ cb, size_t n4,
+                                           size_t tid, size_t stride, const ScalePair sp) {
+  auto code = [&](const float4 &v) {
+    return pack4_fp8<F>(__fmul_rn(v.x, sp.m), __fmul_rn(v.y, sp.m), __fmul_rn(v.z, sp.m), __fmul_rn(v.w, sp.m));
+  };
+  size_t i = tid;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcs(xa + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[4 + u] = __ldcs(xb + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) __stcs(ca + i + u * stride, code(v[u]));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) __stcs(cb + i + u * stride, code(v[4 + u]));
+  }
+  for (; i < n4; i += stride) {
+    __stcs(ca + i, code(__ldcs(xa + i)));
+    __stcs(cb + i, code(__ldcs(xb + i)));
+  }
+}
+
 __global__ void __launch_bounds__(256) k_amax_multi(MultiArgs a, int R, size_t n4, int *status) {
   __shared__ uint32_t red[8];
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (int t = 0; t < R; ++t) {
-    const float4 *x4 = reinterpret_cast<const float4 *>(a.x[t]);
-    uint32_t m = 0;
-    size_t i = tid;
-    for (; i + 3 * stride < n4; i += 4 * stride) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = x4[i + u * stride];   // kept in L2 for the pack pass
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        m = max(m, max(max(abs_bits(v[u].x), abs_bits(v[u].y)), max(abs_bits(v[u].z), abs_bits(v[u].w))));
-    }
-    for (; i < n4; i += stride) {
-      const float4 v = x4[i];
-      m = max(m, max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w))));
-    }
+    uint32_t m = amax_pass(reinterpret_cast<const float4 *>(a.x[t]), n4, tid, stride);
     m = block_max_u32<256>(m, red);
     if (threadIdx.x == 0) {
       if (m) atomicMax(a.amax_bits[t], m);
@@ -152,21 +228,83 @@ __global__ void __launch_bounds__(256) k_pack_tensor_multi(MultiArgs a, int R, s
       a.scale[t][0] = sp.s;
       if (a.amax_out[t]) a.amax_out[t][0] = amax;
     }
-    const float4 *x4 = reinterpret_cast<const float4 *>(a.x[t]);
-    uint32_t *c4 = reinterpret_cast<uint32_t *>(a.codes[t]);
-    auto code = [&](const float4 &v) {
-      return pack4_fp8<F>(__fmul_rn(v.x, sp.m), __fmul_rn(v.y, sp.m), __fmul_rn(v.z, sp.m), __fmul_rn(v.w, sp.m));
-    };
-    size_t i = tid;
-    for (; i + 3 * stride < n4; i += 4 * stride) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * stride);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) c4[i + u * stride] = code(v[u]);
-    }
-    for (; i < n4; i += stride) c4[i] = code(__ldcs(x4 + i));
+    pack_pass<F>(reinterpret_cast<const float4 *>(a.x[t]), reinterpret_cast<uint32_t *>(a.codes[t]), n4, tid,
+                 stride, sp);
   }
+}
+
+// =====================================================================================
+// The replicas of one tensor encoded with one shared scale (the synchronised scale of the
+// Euclidean path: the max over the replicas of their amax) in one cooperative launch: the
+// amax pass over every replica, a grid-wide barrier, then the pack of every replica with the
+// shared amax, last replica first, so that the pack reads first what the amax pass read
+// last and L2 still holds.  Per element the arithmetic is that of the two launches
+// k_amax_multi + k_pack_tensor_multi.  ws[0] (amax bit pattern) and ws[1] (barrier count)
+// are zero on entry.  The barrier wait is bounded: a CTA that gives up sets
+// GIFT_ERR_TIMEOUT and writes no codes.
+// =====================================================================================
+constexpr long long kSharedWait = 2000000000LL;   // clock cycles, about a second
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int F>
+__global__ void __launch_bounds__(256) k_encode_shared(MultiArgs a, int R, size_t n4, uint32_t *ws,
+                                                       float *shared_out, int *status) {
+  __shared__ uint32_t red[8];
+  __shared__ uint32_t amax_sh, ok_sh;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  {
+    int t = 0;
+    for (; t + 1 < R; t += 2)
+      m = max(m, amax_pass2(reinterpret_cast<const float4 *>(a.x[t]), reinterpret_cast<const float4 *>(a.x[t + 1]), n4,
+                            tid, stride));
+    if (t < R) m = max(m, amax_pass(reinterpret_cast<const float4 *>(a.x[t]), n4, tid, stride));
+  }
+  m = block_max_u32<256>(m, red);
+  if (threadIdx.x == 0) {
+    if (m) atomicMax(ws, m);
+    if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + 1) : "memory");
+    uint32_t ok = 1;
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(ws + 1) < gridDim.x) {
+      if (clock64() - t0 > kSharedWait) {
+        ok = 0;
+        set_status(status, GIFT_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    amax_sh = ld_acquire_gpu(ws);
+    ok_sh = ok;
+  }
+  __syncthreads();
+  if (!ok_sh) return;
+  const float amax = __uint_as_float(amax_sh);
+  const ScalePair sp = scale_pair(amax, fmax_of<F>());
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (!(amax <= kF32Max)) set_status(status, GIFT_ERR_NONFINITE);
+    for (int t = 0; t < R; ++t) {
+      a.scale[t][0] = sp.s;
+      if (a.amax_out[t]) a.amax_out[t][0] = amax;
+    }
+    if (shared_out) shared_out[0] = amax;
+  }
+  int t = R - 1;
+  for (; t >= 1; t -= 2)
+    pack_pass2<F>(reinterpret_cast<const float4 *>(a.x[t]), reinterpret_cast<uint32_t *>(a.codes[t]),
+                  reinterpret_cast<const float4 *>(a.x[t - 1]), reinterpret_cast<uint32_t *>(a.codes[t - 1]), n4, tid,
+                  stride, sp);
+  if (t == 0)
+    pack_pass<F>(reinterpret_cast<const float4 *>(a.x[0]), reinterpret_cast<uint32_t *>(a.codes[0]), n4, tid, stride,
+                 sp);
 }
 
 // =====================================================================================
@@ -674,6 +812,34 @@ cudaError_t launch_pack_tensor_multi(const Launch &L, int fmt, const MultiArgs &
   if (fmt == GIFT_FMT_E4M3) k_pack_tensor_multi<FMT_E4M3><<<grid, 256, 0, L.stream>>>(a, R, n / 4, L.status);
   else k_pack_tensor_multi<FMT_E5M2><<<grid, 256, 0, L.stream>>>(a, R, n / 4, L.status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_encode_shared(const Launch &L, int fmt, const MultiArgs &a, int R, size_t n, uint32_t *ws,
+                                 float *shared_out) {
+  const void *kern = (fmt == GIFT_FMT_E4M3) ? reinterpret_cast<const void *>(&k_encode_shared<FMT_E4M3>)
+                                            : reinterpret_cast<const void *>(&k_encode_shared<FMT_E5M2>);
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int grid = stream_grid(L, n / 4, 1024);
+  if (grid > per_sm * L.sms) grid = per_sm * L.sms;   // every CTA resident: the barrier needs it
+  MultiArgs args_a = a;
+  int args_r = R;
+  size_t n4 = n / 4;
+  int *st = L.status;
+  void *args[] = {&args_a, &args_r, &n4, &ws, &shared_out, &st};
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 cudaError_t launch_pack_f32(const Launch &L, const float *x, float *r, size_t n, float *out, float *tout) {

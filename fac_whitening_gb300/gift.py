@@ -74,6 +74,9 @@ def _declare(lib):
                                       ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _sz, _vp, _vp]),
         "gift_amax_replicas": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _vp,
                                     _vp, _sz, _vp, _vp]),
+        "gift_encode_replicas_shared": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), _i, _i, _i, _i,
+                                             _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp,
+                                             _vp, _sz, _vp, _vp]),
         "gift_replica_reduce": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i, _i,
                                      _i, _i, _vp, _vp, _vp]),
         "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
@@ -278,6 +281,19 @@ def gift_encode_replicas(ctx: Context, f: Optional[Factor], Ws: Sequence, fmt: s
                                       PREC[prec], arr(amax_in), arr(codes), arr(scales), arr(tensor_scales),
                                       arr(amax_out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                       _p(status), _stream(stream)), "gift_encode_replicas")
+
+
+def gift_encode_replicas_shared(ctx: Context, f: Optional[Factor], Ws: Sequence, fmt: str, scaling: str,
+                                codes: Sequence, scales: Sequence, tensor_scales: Optional[Sequence] = None,
+                                shared_amax_out=None, prec: str = "fp32", ws=None, status=None, stream=None):
+    R = len(Ws)
+    d_out, d_in = Ws[0].shape
+    arr = lambda xs: (_vp * R)(*[_p(x) for x in xs]) if xs is not None else None  # noqa: E731
+    _check(lib().gift_encode_replicas_shared(ctx.handle, _fptr(f), R, arr(Ws), d_out, d_in, FMT[fmt],
+                                             SCALING[scaling], PREC[prec], arr(codes), arr(scales),
+                                             arr(tensor_scales), _p(shared_amax_out), _p(ws),
+                                             0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                             _stream(stream)), "gift_encode_replicas_shared")
 
 
 def gift_amax_replicas(ctx: Context, f: Optional[Factor], Ws: Sequence, fmt: str, scaling: str, amax_accum,

@@ -273,6 +273,32 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
                                  float *const *tensor_scales, float *const *amax_out, void *ws,
                                  size_t ws_bytes, int *d_status, cudaStream_t stream);
 
+/* Encode R replicas with one shared scale: the amax is the max over the replicas of the amax
+ * each would use on its own (the AllReduceMax of the scale in [notes] Algorithm 1, which the
+ * Euclidean baseline applies on every step), and every replica is packed with it.  The result
+ * is identical to zeroing a word, gift_amax_replicas into it, then gift_encode_replicas with
+ * that word as every replica's amax_in.  The identity transform with per-tensor FP8 scaling
+ * (16-byte aligned gradients, d_out*d_in a multiple of 4, 4-byte aligned codes) is one
+ * cooperative launch: the amax of every replica, a grid-wide barrier, then the pack with the
+ * replicas taken last to first, so that it reads first what the amax pass read last (L2 still
+ * holds up to ~100 MB of it).  Other kinds and formats take the amax launch(es), then the
+ * encode launches of gift_encode_replicas.
+ *  W, codes, scales, tensor_scales : host arrays of R device pointers, each element as in
+ *              gift_encode (tensor_scales only for NVFP4, may be NULL otherwise).
+ *  shared_amax_out : device, 1 float, nullable: the shared amax.
+ *  ws        : gift_workspace_bytes(GIFT_OP_ENCODE, ...).  1 <= R <= 64.
+ * Errors: INVALID_ARG for F32 (no scale) and for block-128 FP8 scaling (the scales are per
+ * block: nothing to share), and for any replica's invalid arguments, before anything is
+ * enqueued.  d_status: NONFINITE; TIMEOUT when the grid-wide barrier wait (bounded at about a
+ * second) gives up, in which case the codes are not written. */
+gift_status gift_encode_replicas_shared(gift_ctx *ctx, const gift_factor *f, int R,
+                                        const float *const *W, int d_out, int d_in,
+                                        gift_format fmt, gift_scaling scaling,
+                                        gift_precision prec, void *const *codes,
+                                        void *const *scales, float *const *tensor_scales,
+                                        float *shared_amax_out, void *ws, size_t ws_bytes,
+                                        int *d_status, cudaStream_t stream);
+
 /* The shared amax of R replicas (the AllReduceMax of the scale in [notes] Algorithm 1, for R
  * workers modelled on one GPU): max-accumulates into amax_accum the amax that gift_amax would
  * give for each of the R tensors W[r] (host array of R device pointers, 1 <= R <= 64).  Same

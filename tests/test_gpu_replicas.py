@@ -5,11 +5,17 @@ the oracle is checked in test_gpu_lowrank.py and test_gpu_codec.py), so every ou
 compared bit for bit: codes, scales, NVFP4 tensor scales, the amax written back, status.
 Shapes: the 600M-like fc2 layer (eight column tiles per CTA), the 300M-like fc2 layer (three
 or four tiles per CTA), a ragged row count, and a narrow layer with one tile per CTA; more
-than 16 replicas take two launches."""
+than 16 replicas take two launches.
+
+gift_encode_replicas_shared (one scale for all replicas) is checked against the oracle (the
+max of the replicas' amax, each replica quantised with it) and, bit for bit, against the
+three steps it stands for: a zeroed word, gift_amax_replicas into it, gift_encode_replicas
+with it as every replica's amax."""
 import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from fac_whitening_gb300 import gift as G
 
 from gpu_util import DEV, alloc_codes, ctx, status, t, ws
@@ -124,7 +130,7 @@ def test_encode_replicas_cached_planes_and_caller_amax(fmt):
 
 @pytest.mark.parametrize("case", ["identity", "block128", "f32"])
 def test_encode_replicas_other_paths(case):
-    # kinds and scalings outside the one-pass kernel: the same as per-replica calls
+    # kinds and scalings outside the batched low-rank kernels: the same as per-replica calls
     f = None if case == "identity" else rand_factor(512, 2048, seed=14)
     fmt = "f32" if case == "f32" else "e4m3"
     scaling = "block128" if case == "block128" else "tensor"
@@ -175,3 +181,114 @@ def test_encode_replicas_identity_shared_amax():
     b = run_single(None, Ws, "e5m2", "tensor", "fp32", amax_in=[shared] * 6)
     assert_same(a, b)
     assert all(o["amax"].item() == shared.item() for o in a[0])
+
+
+# ---- gift_encode_replicas_shared: one scale for all replicas (the synchronised amax) ----------
+
+def shared_outputs(fmt, d_out, d_in, R):
+    outs = outputs(fmt, "tensor", d_out, d_in, R)
+    for o in outs:
+        o["amax"] = None   # no per-replica amax copy in this call
+    return outs
+
+
+def run_shared(f, Ws, fmt, prec="fp32"):
+    d_out, d_in = Ws[0].shape
+    kind = "identity" if f is None else f.kind
+    outs, st = shared_outputs(fmt, d_out, d_in, len(Ws)), status()
+    shared = torch.full((1,), -1.0, device=DEV)
+    G.gift_encode_replicas_shared(ctx(), f, Ws, fmt, "tensor", [o["codes"] for o in outs], [o["scales"] for o in outs],
+                                  tensor_scales=[o["tscale"] for o in outs] if fmt == "nvfp4" else None,
+                                  shared_amax_out=shared, prec=prec, ws=ws("encode", kind, fmt, "tensor", d_out, d_in),
+                                  status=st)
+    torch.cuda.synchronize()
+    return outs, int(st.item()), shared.item()
+
+
+def run_shared_steps(f, Ws, fmt, prec="fp32"):
+    # the same result by its definition: a zeroed word, the replicas' amax max-accumulated
+    # into it, then every replica encoded with that word as its amax
+    d_out, d_in = Ws[0].shape
+    kind = "identity" if f is None else f.kind
+    word = torch.zeros(1, device=DEV)
+    G.gift_amax_replicas(ctx(), f, Ws, fmt, "tensor", word, prec=prec, ws=ws("amax", kind, fmt, "tensor", d_out, d_in))
+    outs, st = shared_outputs(fmt, d_out, d_in, len(Ws)), status()
+    G.gift_encode_replicas(ctx(), f, Ws, fmt, "tensor", [o["codes"] for o in outs], scales=[o["scales"] for o in outs],
+                           tensor_scales=[o["tscale"] for o in outs] if fmt == "nvfp4" else None,
+                           amax_in=[word] * len(Ws), prec=prec, ws=ws("encode", kind, fmt, "tensor", d_out, d_in),
+                           status=st)
+    torch.cuda.synchronize()
+    return outs, int(st.item()), word.item()
+
+
+def spread_replicas(f, R, seed):
+    # replicas whose own amax differ by orders of magnitude, so the shared scale is not theirs
+    Ws = replicas(f, R, seed)
+    for r, W in enumerate(Ws):
+        W.mul_(10.0 ** (r % 4 - 1))
+    return Ws
+
+
+@pytest.mark.parametrize("shape", [(1536, 1536), (1536, 6144), (1000, 2048), (33, 35)], ids=lambda s: f"{s[0]}x{s[1]}")
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_encode_shared_identity_matches_oracle(shape, fmt):
+    # the fused launch (and, for 33x35, whose size is not a multiple of 4, the step sequence)
+    # against the oracle: shared amax = max of the replicas' amax, each replica quantised with it
+    fac = rand_factor(*shape, seed=31, rank=min(32, shape[1]))
+    Ws = spread_replicas(fac, 8, seed=41)
+    outs, st, shared = run_shared(None, Ws, fmt)
+    assert st == 0
+    host = [W.cpu().numpy() for W in Ws]
+    amax = max(O.abs_max(x) for x in host)
+    assert shared == amax
+    for x, o in zip(host, outs):
+        q = O.quantize(x, fmt, amax=amax)
+        np.testing.assert_array_equal(o["codes"].cpu().numpy().reshape(x.shape), q["codes"])
+        assert o["scales"].item() == q["scales"][0]
+    # the small replicas really were coded with the large shared scale
+    assert not np.array_equal(outs[0]["codes"].cpu().numpy().reshape(host[0].shape), O.quantize(host[0], fmt)["codes"])
+
+
+@pytest.mark.parametrize("kind,fmt,prec", [("identity", "e4m3", "fp32"), ("identity", "nvfp4", "fp32"),
+                                           ("lowrank", "e4m3", "fp32"), ("lowrank", "e5m2", "tc"),
+                                           ("lowrank", "nvfp4", "fp32")])
+def test_encode_shared_matches_steps(kind, fmt, prec):
+    fac = rand_factor(1536, 6144, seed=32)
+    f = None if kind == "identity" else fac
+    Ws = spread_replicas(fac, 6, seed=42)
+    (oa, sa, wa), (ob, sb, wb) = run_shared(f, Ws, fmt, prec), run_shared_steps(f, Ws, fmt, prec)
+    assert sa == sb == 0 and wa == wb > 0
+    for x, y in zip(oa, ob):
+        for key in ("codes", "scales", "tscale"):
+            if x[key] is not None:
+                assert torch.equal(x[key], y[key]), key
+
+
+def test_encode_shared_many_replicas_and_zeros():
+    # 64 replicas (the maximum), some of them all zero; and all-zero replicas alone: amax 0,
+    # scale 0, every code +0
+    fac = rand_factor(256, 1024, seed=33)
+    Ws = replicas(fac, 64, seed=43)
+    for r in range(0, 64, 5):
+        Ws[r].zero_()
+    a, b = run_shared(None, Ws, "e4m3"), run_shared_steps(None, Ws, "e4m3")
+    assert a[1] == b[1] == 0 and a[2] == b[2] > 0
+    assert all(torch.equal(x["codes"], y["codes"]) and torch.equal(x["scales"], y["scales"])
+               for x, y in zip(a[0], b[0]))
+    Z = [torch.zeros(256, 1024, device=DEV) for _ in range(3)]
+    outs, st, shared = run_shared(None, Z, "e5m2")
+    assert st == 0 and shared == 0.0
+    assert all(int(o["codes"].count_nonzero()) == 0 and o["scales"].item() == 0.0 for o in outs)
+
+
+def test_encode_shared_nonfinite_and_rejects():
+    fac = rand_factor(512, 2048, seed=34)
+    Ws = replicas(fac, 4, seed=44)
+    Ws[2][7, 9] = float("nan")
+    assert run_shared(None, Ws, "e4m3")[1] == G.ERR_NONFINITE
+    w = ws("encode", "identity", "e4m3", "block128", 512, 2048)
+    outs = shared_outputs("e4m3", 512, 2048, 4)
+    for fmt, scaling in (("e4m3", "block128"), ("f32", "tensor")):
+        with pytest.raises(G.GiftError):
+            G.gift_encode_replicas_shared(ctx(), None, Ws, fmt, scaling, [o["codes"] for o in outs],
+                                          [o["scales"] for o in outs], ws=w)
