@@ -41,3 +41,10 @@ def test_null_context_is_rejected():
     assert lib.gift_create(None, 0) == G.ERR_INVALID_ARG
     assert lib.gift_set_option(None, 0, 10) == G.ERR_INVALID_ARG
     assert lib.gift_workspace_bytes(None, 1, 0, 1, 0, 4, 4, 0, 0) == ctypes.c_size_t(-1).value
+    # the replica entry points check their context before anything else (no CUDA call)
+    assert lib.gift_encode_replicas(None, None, 1, None, 4, 4, 1, 0, 0, None, None, None, None, None, None, 0,
+                                    None, None) == G.ERR_INVALID_ARG
+    assert lib.gift_encode_replicas_shared(None, None, 1, None, 4, 4, 1, 0, 0, None, None, None, None, None, 0,
+                                           None, None) == G.ERR_INVALID_ARG
+    assert lib.gift_amax_replicas(None, None, 1, None, 4, 4, 1, 0, 0, None, None, 0, None, None) == G.ERR_INVALID_ARG
+    assert lib.gift_replica_reduce(None, 1, None, None, None, 1, 0, 4, 4, None, None, None) == G.ERR_INVALID_ARG
