@@ -3,8 +3,11 @@
 // Each entry point validates its arguments on the host, carves the caller's workspace
 // with the same layout function that gift_workspace_bytes uses, and enqueues kernels on
 // the caller's stream.  No call allocates or frees device memory and no call synchronises.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <numeric>
+#include <vector>
 
 #include "kernels.cuh"
 
@@ -917,6 +920,44 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
   CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
   CK(launch_amax(L, W, nullptr, n, w.amax));
   CK(launch_hits_tensor(L, fmt, W, n, w.amax, d_counts));
+  return GIFT_OK;
+}
+
+// Fragile-layer selection from a profiling window (host only).  Scores are formed in double
+// from the integer counts, so every comparison below is exact and repeatable.
+gift_status gift_select_fragile(int L, const unsigned long long *counts, int k, int k_min, int k_max, int *order,
+                                double *scores, int *k_out) {
+  if (L < 1 || !counts || !order || !k_out || k < 0 || k > L) return GIFT_ERR_INVALID_ARG;
+  if (k == 0 && !(1 <= k_min && k_min <= k_max && k_max <= L)) return GIFT_ERR_INVALID_ARG;
+  std::vector<double> s(L);
+  for (int l = 0; l < L; ++l) {
+    const unsigned long long up = counts[3 * (size_t)l], lo = counts[3 * (size_t)l + 1],
+                             n = counts[3 * (size_t)l + 2];
+    if (up > n || lo > n) return GIFT_ERR_INVALID_ARG;   // not the counts of one layer
+    s[l] = n ? (double)(up + lo) / (double)n : 0.0;
+  }
+  std::vector<int> o(L);
+  std::iota(o.begin(), o.end(), 0);
+  std::sort(o.begin(), o.end(), [&](int a, int b) { return s[a] > s[b] || (s[a] == s[b] && a < b); });
+  if (k == 0) {
+    k = k_min;
+    if (k_min < L) {
+      // the largest drop between consecutive ranked scores; equal drops keep the smaller k
+      const int hi = std::min(k_max, L - 1);
+      double best = s[o[k_min - 1]] - s[o[k_min]];
+      for (int c = k_min + 1; c <= hi; ++c) {
+        const double drop = s[o[c - 1]] - s[o[c]];
+        if (drop > best) {
+          best = drop;
+          k = c;
+        }
+      }
+    }
+  }
+  for (int i = 0; i < L; ++i) order[i] = o[i];
+  if (scores)
+    for (int l = 0; l < L; ++l) scores[l] = s[l];
+  *k_out = k;
   return GIFT_OK;
 }
 

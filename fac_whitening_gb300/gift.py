@@ -77,6 +77,7 @@ def _declare(lib):
         "gift_encode_replicas_shared": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), _i, _i, _i, _i,
                                              _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp,
                                              _vp, _sz, _vp, _vp]),
+        "gift_select_fragile": (_i, [_i, _vp, _i, _i, _i, _vp, _vp, _vp]),
         "gift_replica_reduce": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i, _i,
                                      _i, _i, _vp, _vp, _vp]),
         "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
@@ -179,6 +180,24 @@ def gift_code_sizes(fmt: str, scaling: str, d_out: int, d_in: int):
     _check(lib().gift_code_sizes(FMT[fmt], SCALING[scaling], d_out, d_in, ctypes.byref(cb), ctypes.byref(sc)),
            "gift_code_sizes")
     return cb.value, sc.value
+
+
+def gift_select_fragile(counts, k: int = 0, k_min: int = 1, k_max: Optional[int] = None):
+    """Host-side layer selection from window counts (L x 3: upper, lower, n per layer).
+    Returns (order, scores, k): layer indices by descending score, the scores, and how many
+    of order are selected (k > 0: that many; k = 0: at the knee within [k_min, k_max])."""
+    flat = [int(v) for row in counts for v in row]
+    L = len(flat) // 3
+    if L * 3 != len(flat):
+        raise ValueError("counts must be L rows of (upper, lower, n)")
+    c = (ctypes.c_ulonglong * max(len(flat), 1))(*flat)
+    order = (ctypes.c_int * max(L, 1))()
+    scores = (ctypes.c_double * max(L, 1))()
+    k_out = ctypes.c_int()
+    _check(lib().gift_select_fragile(L, ctypes.cast(c, _vp), k, k_min, L if k_max is None else k_max,
+                                     ctypes.cast(order, _vp), ctypes.cast(scores, _vp), ctypes.byref(k_out)),
+           "gift_select_fragile")
+    return list(order)[:L], list(scores)[:L], k_out.value
 
 
 # ---- factor -------------------------------------------------------------------------------

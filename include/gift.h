@@ -348,6 +348,29 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
                                    unsigned long long *d_counts, void *ws, size_t ws_bytes,
                                    int *d_status, cudaStream_t stream);
 
+/* Fragile-layer selection after a profiling window ([notes] simplification 3: boundary-hit
+ * rates averaged over the profiling window, upper and lower rates summed into a fragility
+ * score; the geometry-aware branch goes to the layers before the clear drop in that score).
+ * Host only (no context, no device).
+ *  L       : number of layers, >= 1.
+ *  counts  : host, L x 3 unsigned 64-bit: layer l's (upper, lower, n) summed over the window,
+ *            as gift_boundary_hit_rate accumulates them.  n is the layer's element count at
+ *            each step times the steps, so upper + lower over n is the window mean of the
+ *            per-step rate.  upper <= n and lower <= n, else INVALID_ARG.
+ *  k       : > 0: select the k highest-scoring layers.  0: select at the knee, the k in
+ *            [k_min, min(k_max, L - 1)] with the largest drop between consecutive ranked
+ *            scores (equal drops: the smaller k); with k_min = L, all L.
+ *            1 <= k_min <= k_max <= L is required when k = 0; otherwise both are ignored.
+ *  order   : host, L ints out: layer indices by descending score, ties to the lower index.
+ *            The selected layers are order[0 .. *k_out).
+ *  scores  : host, L doubles out (nullable): (upper + lower) / n per layer in double,
+ *            0 when n = 0.
+ *  k_out   : host, 1 int out.
+ * Errors (INVALID_ARG, nothing written): L < 1, null counts/order/k_out, k outside [0, L],
+ * a bad k_min/k_max with k = 0, counts above n. */
+gift_status gift_select_fragile(int L, const unsigned long long *counts, int k, int k_min, int k_max,
+                                int *order, double *scores, int *k_out);
+
 /* Rank-r encode that allocates nothing (the paper has no counterpart; this is a library
  * convenience).  Same result as gift_encode with a LOWRANK factor, E4M3 or E5M2 and
  * per-tensor scaling, but without a caller workspace: for callers that cannot allocate

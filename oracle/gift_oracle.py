@@ -400,6 +400,42 @@ def select_fragile(scores, k):
     return order[:k]
 
 
+def window_scores(counts):
+    """Fragility score of every layer over a profiling window (the profiling procedure of
+    simplification 3: boundary-hit rates averaged over the window, upper and lower summed).
+    counts[l] = (upper, lower, n) summed over the window's steps.  A layer's element count
+    is the same at every step, so the window mean of the per-step rate (upper + lower) / n
+    is the summed hits over the summed n."""
+    return [fragility_score(c) for c in counts]
+
+
+def knee_count(ranked, k_min=1, k_max=None):
+    """The number of layers before the clear drop in score (simplification 3, Figure 3: the
+    fragile group, then a marked drop).  Reading: over k in [k_min, min(k_max, L - 1)],
+    the k with the largest drop ranked[k-1] - ranked[k] between consecutive scores in
+    descending order; equal drops go to the smaller k.  With one layer, or k_min = L, the
+    answer is L."""
+    L = len(ranked)
+    k_max = L if k_max is None else k_max
+    if not 1 <= k_min <= k_max <= L:
+        raise ValueError("need 1 <= k_min <= k_max <= number of layers")
+    if k_min == L:
+        return L
+    best_k, best = k_min, None
+    for k in range(k_min, min(k_max, L - 1) + 1):
+        drop = ranked[k - 1] - ranked[k]
+        if best is None or drop > best:
+            best_k, best = k, drop
+    return best_k
+
+
+def select_fragile_knee(scores, k_min=1, k_max=None):
+    """Layer indices by descending score (ties to the lower index), cut at the knee."""
+    order = sorted(range(len(scores)), key=lambda i: (-scores[i], i))
+    k = knee_count([scores[i] for i in order], k_min, k_max)
+    return order[:k]
+
+
 # ======================================================================================
 # K-FAC factors ([notes] 前置知识 "K-FAC", eq. (4): A = E[a a^T], G = E[delta delta^T])
 # ======================================================================================
