@@ -110,10 +110,17 @@ def header_functions():
 
 
 def _p(t) -> Optional[int]:
+    """Address of a caller buffer for the library: None, a raw device address (int), or a
+    contiguous CUDA tensor.  A host tensor or a strided view is refused here, since a kernel
+    would read it as contiguous device memory."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not getattr(t, "is_cuda", False):
+        raise ValueError("libgift buffers live in device memory: pass a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("libgift buffers are dense row-major: pass a contiguous tensor")
     return t.data_ptr()
 
 

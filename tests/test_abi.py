@@ -48,3 +48,29 @@ def test_null_context_is_rejected():
                                            None, None) == G.ERR_INVALID_ARG
     assert lib.gift_amax_replicas(None, None, 1, None, 4, 4, 1, 0, 0, None, None, 0, None, None) == G.ERR_INVALID_ARG
     assert lib.gift_replica_reduce(None, 1, None, None, None, 1, 0, 4, 4, None, None, None) == G.ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_and_strided_buffers():
+    # the binding hands the library device addresses of dense buffers only
+    import torch
+
+    assert G._p(None) is None and G._p(1234) == 1234
+    with pytest.raises(ValueError, match="device memory"):
+        G._p(torch.zeros(4))
+
+    class StridedCuda:   # stands in for a CUDA tensor view (no GPU here)
+        is_cuda = True
+
+        def is_contiguous(self):
+            return False
+
+        def data_ptr(self):
+            return 4096
+
+    class DenseCuda(StridedCuda):
+        def is_contiguous(self):
+            return True
+
+    with pytest.raises(ValueError, match="contiguous"):
+        G._p(StridedCuda())
+    assert G._p(DenseCuda()) == 4096
