@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -196,7 +197,9 @@ class ClockSampler:
     def __init__(self, index):
         self.proc = None
         self.index = index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples (the JSON line carries their summary); GIFT_BENCH_CLOCKS_DIR keeps them
+        out_dir = os.environ.get("GIFT_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"gift_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
