@@ -202,6 +202,9 @@ class ClockSampler:
         self.path = os.path.join(out_dir, f"gift_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        import shutil
+        if shutil.which("nvidia-smi") is None:   # nothing to sample on this machine
+            return self
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
