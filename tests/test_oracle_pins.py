@@ -285,6 +285,15 @@ def test_kfac_factor_matches_outer_products():
     np.testing.assert_allclose(O.kfac_factor(a), A, rtol=1e-14, atol=1e-15)
 
 
+def test_global_factor_is_the_stacked_factor():
+    # the replica-averaged factor (1/R) sum_r a_r^T a_r / T, for replicas of equal T, is the
+    # factor of the replicas' activations stacked into one batch of R T rows
+    rng = np.random.default_rng(12)
+    acts = [rng.standard_normal((16, 5)) * (1 + r) for r in range(4)]
+    mean = sum(O.kfac_factor(x) for x in acts) / len(acts)
+    np.testing.assert_allclose(O.kfac_factor(np.concatenate(acts)), mean, rtol=1e-13, atol=1e-14)
+
+
 def test_cholesky_vs_lapack_and_identities():
     A = _spd(24, 1)
     L = O.cholesky(A)
