@@ -74,3 +74,25 @@ def test_binding_refuses_host_and_strided_buffers():
     with pytest.raises(ValueError, match="contiguous"):
         G._p(StridedCuda())
     assert G._p(DenseCuda()) == 4096
+
+
+def _header_param_counts():
+    import re
+    text = open(G.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    counts = {}
+    for m in re.finditer(r"(gift_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, re.S):
+        params = m.group(2).strip()
+        counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_declares_every_function_with_the_header_arity():
+    # every declared function has a ctypes signature, with as many arguments as the header's
+    lib = _lib_or_skip()
+    counts = _header_param_counts()
+    assert set(counts) == set(G.header_functions())
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no ctypes signature"
+        assert len(fn.argtypes) == n, f"{name}: {len(fn.argtypes)} ctypes arguments, header has {n}"
