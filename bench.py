@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -83,6 +84,20 @@ def max_over_ranks(x, world, device):
 def job_value(world, bytes_per_rank, ms):
     """Whole-job throughput in GB/s: every rank codes its own replicas (weak scaling)."""
     return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
+def fidelity_stats(g_hat, g):
+    """RelL2, Cos, MaxErr and MSE of a decoded gradient against the FP32 mean of the replica
+    gradients, in float64 (the fidelity measures of the GIFT reading notes, simplification 1,
+    eq. (15))."""
+    import torch
+    gh = g_hat.double().reshape(-1)
+    gg = g.double().reshape(-1)
+    e = gh - gg
+    ng, nh = torch.linalg.norm(gg), torch.linalg.norm(gh)
+    fin = lambda x: float(x) if math.isfinite(float(x)) else None   # noqa: E731  (strict JSON)
+    return {"rel_l2": fin(torch.linalg.norm(e) / ng), "cos": fin(torch.dot(gh, gg) / (nh * ng)),
+            "max_err": fin(e.abs().max()), "mse": fin(torch.dot(e, e) / e.numel())}
 
 
 def solo_call_ms(graph, calls, reps):
@@ -476,6 +491,30 @@ def main_gift(args):
                 for i, (name, _) in enumerate(graphs)}
     value = job_value(world, grad_bytes, ms)
 
+    # ---- fidelity of one geometry-aware layer (after the timed region) -----------------
+    # the decoded layer against the FP32 mean of its replicas, and the same replicas through
+    # the Euclidean codec (shared scale) for comparison
+    try:
+        L0 = gl[0]
+        gbar = torch.zeros(d_out, d_in, dtype=torch.float64, device=dev)
+        for W in L0["W"]:
+            gbar += W.double()
+        gbar /= len(L0["W"])
+        fid = {"gift": fidelity_stats(L0["out"], gbar)}
+        ecodes = [torch.empty_like(c) for c in L0["codes"]]
+        escales = [torch.empty_like(x) for x in L0["scales"]]
+        eavg = torch.empty_like(L0["avg"])
+        fst = torch.zeros(1, dtype=torch.int32, device=dev)
+        G.gift_encode_replicas_shared(ctx, None, L0["W"], FMT, "tensor", ecodes, escales, ws=wss[0], status=fst)
+        G.gift_replica_reduce(ctx, ecodes, escales, FMT, "tensor", d_out, d_in, eavg, status=fst)
+        torch.cuda.synchronize()
+        fid["euclid_same_layer"] = fidelity_stats(eavg, gbar)
+        fid["device_status"] = int(fst.item())
+        fid["layer"] = f"fc2.0 {d_out}x{d_in}, R={R}, {FMT} per-tensor"
+        del ecodes, escales, eavg, gbar
+    except Exception as ex:   # a measurement, never a reason to lose the bench line
+        fid = {"error": str(ex)[:200]}
+
     # ---- roofline of the dominant kernel ----------------------------------------------
     # The dominant group is the Euclidean shared-scale encode (one cooperative launch per
     # tensor: amax of its R replicas, grid barrier, pack) or the rank-r encode (one
@@ -538,7 +577,7 @@ def main_gift(args):
                            "gradient_bytes_per_step": grad_bytes, "l2": "inputs exceed L2 (no flush)",
                            "parallelism": f"replicas x{world}", "streams_per_stage": nstr},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": kernels_per_step * args.steps, "stages": stages,
+                "gpu_launches": kernels_per_step * args.steps, "stages": stages, "fidelity": fid,
                 "factor_syrk": kfac,
                 "factor_refresh": {p: {"ms_per_layer": ms_, "syrk_tflops": syrk_flops / (ms_ * 1e-3) / 1e12}
                                    for p, ms_ in refresh.items()} | {
