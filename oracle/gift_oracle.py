@@ -265,6 +265,39 @@ def dequantize_block128(codes, scales, fmt: Fmt) -> np.ndarray:
     return out
 
 
+# 1-D blocks: the per-block Euclidean baseline of the experiments (block size 512).  Reading:
+# one FP32 scale per 512 consecutive elements of the row-major flattened tensor, the last
+# block shorter when the element count is not a multiple of 512.
+BLOCK1D = 512
+
+
+def quantize_block1d(x, fmt: Fmt, amax=None, b=BLOCK1D):
+    """Returns (codes, scales[nb], amax[nb]), nb = ceil(n / b); amax overrides the blocks'
+    own (one value per block)."""
+    x = np.asarray(x, dtype=np.float32)
+    flat = x.ravel()
+    nb = (flat.size + b - 1) // b
+    codes = np.zeros(flat.size, dtype=np.uint8)
+    scales = np.zeros(nb, dtype=np.float32)
+    am = np.zeros(nb, dtype=np.float32)
+    for i in range(nb):
+        blk = flat[i * b:(i + 1) * b]
+        am[i] = abs_max(blk) if amax is None else F32(np.asarray(amax).ravel()[i])
+        s, m = scale_pair(am[i], fmt)
+        scales[i] = s
+        codes[i * b:(i + 1) * b] = quantize_with_multiplier(blk, m, fmt)
+    return codes.reshape(x.shape), scales, am
+
+
+def dequantize_block1d(codes, scales, fmt: Fmt, b=BLOCK1D) -> np.ndarray:
+    codes = np.asarray(codes)
+    flat = codes.ravel()
+    out = np.zeros(flat.size, dtype=np.float32)
+    for i in range(len(scales)):
+        out[i * b:(i + 1) * b] = dequantize(flat[i * b:(i + 1) * b], scales[i], fmt)
+    return out.reshape(codes.shape)
+
+
 # ======================================================================================
 # NVFP4 ([abstract]: "FP8 and NVFP4"; the layout below is the plain public reading:
 # E2M1 codes, one E4M3 scale per 16 consecutive elements of a row, one FP32 tensor scale)
@@ -340,6 +373,9 @@ def quantize(x, fmt: str, scaling: str = "tensor", amax=None):
     if scaling == "tensor":
         c, s, a = quantize_tensor(x, f, amax)
         return {"codes": c, "scales": np.array([s], dtype=np.float32), "tensor_scale": None, "amax": a}
+    if scaling == "block512":
+        c, s, a = quantize_block1d(x, f, amax)
+        return {"codes": c, "scales": s, "tensor_scale": None, "amax": a}
     c, s, a = quantize_block128(x, f, amax)
     return {"codes": c, "scales": s, "tensor_scale": None, "amax": a}
 
@@ -352,6 +388,8 @@ def dequantize_any(q, fmt: str, scaling: str = "tensor") -> np.ndarray:
     f = FORMATS[fmt]
     if scaling == "tensor":
         return dequantize(q["codes"], q["scales"][0], f)
+    if scaling == "block512":
+        return dequantize_block1d(q["codes"], q["scales"], f)
     return dequantize_block128(q["codes"], q["scales"], f)
 
 

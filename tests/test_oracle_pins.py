@@ -266,6 +266,45 @@ def test_boundary_hits_brute_force():
         assert O.boundary_hits(x, name) == (up, lo, x.size)
 
 
+def test_block1d_single_block_is_per_tensor():
+    x = np.random.default_rng(40).standard_normal((20, 25)).astype(np.float32)   # 500 elements
+    for name in ("e4m3", "e5m2"):
+        c, s, a = O.quantize_block1d(x, OFMT[name])
+        ct, st, at = O.quantize_tensor(x, OFMT[name])
+        np.testing.assert_array_equal(c, ct)
+        assert s.shape == (1,) and s[0] == st and a[0] == at
+
+
+def test_block1d_power_of_two_copies():
+    # blocks that are power-of-two multiples of one block: identical codes, scales in the
+    # same ratios exactly; a block boundary off by any amount mixes scales and breaks this
+    base = np.random.default_rng(41).standard_normal(512).astype(np.float32)
+    ks = [-3, 0, 2, 5]
+    x = np.stack([base * np.float32(2.0 ** k) for k in ks]).reshape(8, 256)
+    for name in ("e4m3", "e5m2"):
+        c, s, _ = O.quantize_block1d(x, OFMT[name])
+        blocks = c.reshape(4, 512)
+        for i in range(4):
+            np.testing.assert_array_equal(blocks[i], blocks[1])
+            assert s[i] == s[1] * np.float32(2.0 ** ks[i])
+
+
+def test_block1d_ragged_tail_and_roundtrip():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((10, 100)).astype(np.float32)      # 1000 elements: 512 + 488
+    x.ravel()[900] = 1000.0                                     # an outlier in the short block
+    q = O.quantize(x, "e4m3", "block512")
+    assert q["scales"].shape == (2,)
+    ct, st, _ = O.quantize_tensor(x.ravel()[:512], OFMT["e4m3"])
+    np.testing.assert_array_equal(q["codes"].ravel()[:512], ct)
+    assert q["scales"][0] == st and q["scales"][1] == np.float32(1000.0) / np.float32(448.0)
+    # round trip within half a code step of the scaled value, plus the subnormal step
+    xh = O.dequantize_any(q, "e4m3", "block512")
+    s_el = np.repeat(q["scales"], 512)[:1000].reshape(x.shape).astype(np.float64)
+    bound = np.abs(x) * 2.0 ** -4 + O.FORMATS["e4m3"].min_subnormal * s_el
+    assert np.all(np.abs(xh.astype(np.float64) - x) <= bound * 1.0001)
+
+
 def test_select_fragile_ties():
     assert O.select_fragile([0.1, 0.3, 0.3, 0.05, 0.2], 3) == [1, 2, 4]
 
