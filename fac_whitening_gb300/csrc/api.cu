@@ -735,8 +735,10 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
   return GIFT_OK;
 }
 
-// Two workspace amax words beyond those of the batched rank-r encode and of the replicas'
-// own amax: the shared amax and the barrier count of the shared-scale encode.
+// Workspace control words 62 and 63: the shared amax and the barrier count of the
+// shared-scale encode.  Nothing else in that call touches them: the batched rank-r encode
+// uses words 0-16, and the replicas are encoded with the shared word as their amax, so no
+// replica's own-amax word is used.
 constexpr int kSharedAmaxWord = 62;
 
 gift_status gift_encode_replicas_shared(gift_ctx *ctx, const gift_factor *f, int R, const float *const *W,
