@@ -131,3 +131,29 @@ def test_library_rejects_bad_arguments():
         G.gift_select_fragile([(101, 0, 100)])     # more hits than elements
     with pytest.raises(G.GiftError):
         G.gift_select_fragile([])                   # no layers
+
+
+def test_window_of_heavy_tailed_layers_end_to_end():
+    # a 5-step profiling window over 12 heavy-tailed layers (the profiler workload's kind of
+    # tensor, small shapes; half the layers with a much wider column spread, the "fragile"
+    # ones): counts summed with the oracle's boundary-hit rule, then the library's selection
+    # must equal the oracle's, in both formats
+    _lib_or_skip()
+    from fac_whitening_gb300 import synth
+    for fmt in ("e4m3", "e5m2"):
+        window = [[0, 0, 0] for _ in range(12)]
+        for step in range(5):
+            for layer in range(12):
+                spread = 4.0 if layer % 2 else 1.0
+                W = synth.student_t_colscaled(48, 64, seed=1000 * step + layer, col_sigma=spread).numpy()
+                up, lo, n = O.boundary_hits(W, fmt)
+                window[layer][0] += up
+                window[layer][1] += lo
+                window[layer][2] += n
+        order, scores, k = G.gift_select_fragile(window)
+        want = O.window_scores(window)
+        assert scores == want
+        assert order[:k] == O.select_fragile_knee(want)
+        assert k >= 1 and all(s > 0 for s in scores)
+        if fmt == "e4m3":   # E4M3's narrow range: the knee picks exactly the wide-spread layers
+            assert sorted(order[:k]) == [1, 3, 5, 7, 9, 11]
