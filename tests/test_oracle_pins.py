@@ -305,6 +305,25 @@ def test_block1d_ragged_tail_and_roundtrip():
     assert np.all(np.abs(xh.astype(np.float64) - x) <= bound * 1.0001)
 
 
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "tensor"), ("e4m3", "block128"),
+                                         ("e5m2", "block512"), ("nvfp4", "tensor")])
+def test_quantisers_are_power_of_two_equivariant(fmt, scaling):
+    # scaling a tensor by 2^k scales amax, s and every block amax by 2^k exactly and leaves
+    # every scaled value x * m unchanged: the codes must not move and the stored scales must
+    # scale exactly (the NVFP4 block scales are ratios of amaxes and must not move either)
+    x = np.random.default_rng(43).standard_normal((200, 320)).astype(np.float32)
+    x[3, :7] = 0
+    q0 = O.quantize(x, fmt, scaling)
+    for k in (-20, -3, 5, 30):
+        qk = O.quantize(x * np.float32(2.0 ** k), fmt, scaling)
+        np.testing.assert_array_equal(qk["codes"], q0["codes"])
+        if fmt == "nvfp4":
+            np.testing.assert_array_equal(qk["scales"], q0["scales"])
+            assert qk["tensor_scale"] == q0["tensor_scale"] * np.float32(2.0 ** k)
+        else:
+            np.testing.assert_array_equal(qk["scales"], q0["scales"] * np.float32(2.0 ** k))
+
+
 def test_select_fragile_ties():
     assert O.select_fragile([0.1, 0.3, 0.3, 0.05, 0.2], 3) == [1, 2, 4]
 
