@@ -324,6 +324,25 @@ def test_quantisers_are_power_of_two_equivariant(fmt, scaling):
             np.testing.assert_array_equal(qk["scales"], q0["scales"] * np.float32(2.0 ** k))
 
 
+def test_transforms_are_homogeneous_in_the_factor():
+    # A -> c A: T_A -> c^-1/2 T_A (whitening scales by c^-1/2, map-back by c^1/2), for the
+    # sigma-completed rank-r factor and for the Cholesky factor (L -> c^1/2 L)
+    rng = np.random.default_rng(44)
+    W = rng.standard_normal((6, 40))
+    X = rng.standard_normal((6, 40))
+    A = _spd(40, 7)
+    F = O.lowrank_factor_from_A(A, r=8)
+    c = 9.0
+    Fc = O.LowRankFactor(F.U, F.mu * c, F.sigma * c)
+    np.testing.assert_allclose(O.lowrank_whiten(W, Fc), O.lowrank_whiten(W, F) / 3.0, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(O.lowrank_unwhiten(X, Fc), O.lowrank_unwhiten(X, F) * 3.0, rtol=1e-12, atol=1e-14)
+    L = O.cholesky(A)
+    np.testing.assert_allclose(O.cholesky(c * A), 3.0 * L, rtol=1e-12, atol=1e-14)
+    xf, xfc = O.Xform("chol_input", LA=L), O.Xform("chol_input", LA=3.0 * L)
+    np.testing.assert_allclose(xfc.whiten(W), xf.whiten(W) / 3.0, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(xfc.unwhiten(X), xf.unwhiten(X) * 3.0, rtol=1e-12, atol=1e-14)
+
+
 def test_select_fragile_ties():
     assert O.select_fragile([0.1, 0.3, 0.3, 0.05, 0.2], 3) == [1, 2, 4]
 
