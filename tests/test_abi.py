@@ -1,5 +1,6 @@
 """The C ABI library loads on a CPU-only machine and exports every declared function."""
 import ctypes
+import os
 
 import pytest
 
@@ -96,3 +97,37 @@ def test_binding_declares_every_function_with_the_header_arity():
         fn = getattr(lib, name)
         assert fn.argtypes is not None, f"{name}: no ctypes signature"
         assert len(fn.argtypes) == n, f"{name}: {len(fn.argtypes)} ctypes arguments, header has {n}"
+
+
+def test_c_program_links_and_calls_host_entry_points(tmp_path):
+    # the boundary is a C ABI: a C99 program includes gift.h, links libgift.so and calls the
+    # host-only entry points (no device needed)
+    import shutil
+    import subprocess
+    _lib_or_skip()
+    cuda_inc = "/usr/local/cuda/include"
+    if shutil.which("gcc") is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = tmp_path / "consumer.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "gift.h"
+int main(void) {
+  size_t cb = 0, sc = 0;
+  unsigned long long counts[6] = {1, 9, 100, 0, 1, 100};
+  int order[2] = {-1, -1}, k = -1;
+  double scores[2];
+  if (gift_code_sizes(GIFT_FMT_NVFP4, GIFT_SCALE_TENSOR, 4, 32, &cb, &sc) != GIFT_OK) return 2;
+  if (gift_select_fragile(2, counts, 1, 1, 2, order, scores, &k) != GIFT_OK) return 3;
+  printf("%d %zu %zu %d %d %d %s\n", gift_version(), cb, sc, order[0], order[1], k,
+         gift_status_string(GIFT_ERR_INVALID_ARG));
+  return 0;
+}
+""")
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(G.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", f"-I{os.path.dirname(G.HEADER)}", f"-I{cuda_inc}",
+                    str(src), "-o", str(exe), f"-L{libdir}", "-lgift", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out[:6] == ["1", "64", "8", "0", "1", "1"]
+    assert " ".join(out[6:]) == G.status_string(G.ERR_INVALID_ARG)
