@@ -152,8 +152,8 @@ def peaks():
 # --------------------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same workload
 # --------------------------------------------------------------------------------------
-def oracle_sample_step(sample):
-    import oracle as O
+def oracle_sample_step(sample, O):
+    """One codec pass of the sample through the oracle statement O (oracle.cpp or numpy)."""
     W_g, W_e, F = sample["gift"], sample["euclid"], sample["factor"]
     xf = O.Xform("lowrank", F=F)
     qs = [O.encode_layer(W, xf, FMT)[0] for W in W_g]
@@ -164,43 +164,72 @@ def oracle_sample_step(sample):
     O.replica_reduce(qe, FMT)
 
 
-def make_oracle_sample(rows=1536, R=8):
+def make_oracle_sample(rows, R=8):
     """One geometry-aware layer and one Euclidean tensor, `rows` x 6144, R replicas (CPU)."""
-    import numpy as np
     import torch
-    import oracle as O
+    import oracle.cpp as OC
     from fac_whitening_gb300 import synth
     spec = synth.LayerSpec("sample", rows, 6144, T=2048, exponent=1.0)
     Ws, a = synth.layer_inputs(spec, 2, 77, R, device="cpu")
-    F = O.lowrank_factor_from_activations(a.to(torch.float64).numpy(), r=32, iters=8)
+    F = OC.lowrank_factor_from_activations(a.to(torch.float64).numpy(), r=32, iters=8)
     We = [synth.gaussian((rows, 6144), synth.seed_for(2, 99, r)).numpy() for r in range(R)]
     nbytes = 2 * R * rows * 6144 * 4
     return {"gift": [W.numpy() for W in Ws], "euclid": We, "factor": F, "bytes": nbytes,
-            "desc": f"one 1536x6144 fc2 layer and one Euclidean 1536x6144 tensor, first {rows} rows, R={R}"}
+            "desc": f"one 600M-like fc2 layer ({rows}x6144 rows of 1536x6144, rank 32) and one Euclidean "
+                    f"{rows}x6144 tensor, R={R}: encode, reduce, decode"}
 
 
 def cpu_cores():
     return os.cpu_count() or 1
 
 
+def time_oracle(sample, steps, warmup=0, openmp=False):
+    """Seconds per step of the C++ oracle: single-threaded and pinned to one host core
+    (taskset -c <core>), or the OpenMP build of the same source on every core this process may
+    use.  Returns (seconds, threads)."""
+    import oracle.cpp as OC
+    allowed = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    threads = OC.use_openmp(openmp)
+    try:
+        if not openmp and allowed:
+            os.sched_setaffinity(0, {min(allowed)})
+        for _ in range(warmup):
+            oracle_sample_step(sample, OC)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            oracle_sample_step(sample, OC)
+        dt = (time.perf_counter() - t0) / max(steps, 1)
+    finally:
+        if allowed:
+            os.sched_setaffinity(0, allowed)
+        OC.use_openmp(False)
+    return dt, threads
+
+
+def cpu_baseline_entry(sample, dt, threads, omp=None):
+    e = {"value": sample["bytes"] / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+         "sample": sample["desc"], "seconds": dt,
+         "oracle": "plain C++17 (oracle/gift_oracle.cpp), -O2 -ffp-contract=off, one thread pinned to one core"}
+    if omp is not None:
+        odt, othreads = omp
+        e["all_cores"] = {"value": sample["bytes"] / odt / 1e9, "unit": UNIT, "cores": othreads, "seconds": odt,
+                          "oracle": "the same source built with OpenMP"}
+    return e
+
+
 def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    sample = make_oracle_sample()
-    for _ in range(args.warmup):
-        oracle_sample_step(sample)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_sample_step(sample)
-    dt = (time.perf_counter() - t0) / args.steps
+    # each step is a bounded sample, so that --steps K --warmup W ends within a few minutes
+    sample = make_oracle_sample(rows=256)
+    dt, threads = time_oracle(sample, args.steps, args.warmup)
     value = sample["bytes"] / dt / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 transform, f32 quantiser", "data": "synthetic",
             "config": {"workload": "llama600m-selective (oracle sample)", "sample": sample["desc"]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample["desc"]},
+            "cpu_baseline": cpu_baseline_entry(sample, dt, threads),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -559,12 +588,9 @@ def main_gift(args):
     # ---- CPU baseline (oracle on a bounded sample) --------------------------------------
     cpu = None
     if not args.no_cpu_baseline and rank == 0:
-        sample = make_oracle_sample()
-        t_a = time.perf_counter()
-        oracle_sample_step(sample)
-        dt = time.perf_counter() - t_a
-        cpu = {"value": sample["bytes"] / dt / 1e9, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": sample["desc"], "seconds": dt}
+        sample = make_oracle_sample(rows=768)   # about 15 s of single-core work
+        dt, threads = time_oracle(sample, 1)
+        cpu = cpu_baseline_entry(sample, dt, threads, omp=time_oracle(sample, 1, warmup=1, openmp=True))
 
     if rank == 0:
         clocks = clk.summary()

@@ -26,7 +26,8 @@ namespace {
 
 constexpr int kNoAllocMaxRows = 4096;                        // d_out limit
 constexpr int kNoAllocMaxCols = 16384;                       // d_in limit
-constexpr size_t kNoAllocAmaxFloats = 64;                    // one word, padded to 256 B
+constexpr size_t kNoAllocAmaxFloats = 64;                    // amax words and the barrier word, padded to 256 B
+static_assert(gift::kEncodeBatchMax + 1 <= kNoAllocAmaxFloats, "the amax words and the barrier word fit the control block");
 constexpr size_t kNoAllocPcFloats = (size_t)kNoAllocMaxRows * 32;
 constexpr size_t kNoAllocPartFloats = (size_t)2 << 20;       // 8 MiB of projection partials
 // tensor-core operand planes and counters (the lr_pipe_split_floats layout at the limits)
@@ -106,7 +107,7 @@ extern "C" gift_status gift_encode_lowrank_noalloc(gift_ctx *ctx, const gift_fac
   a.amax_out = amax_out;
   a.amax_in = amax_in;
   a.amax_ws = amax_ws;
-  a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + 16);
+  a.grid_counter = reinterpret_cast<unsigned int *>(amax_ws + kEncodeBatchMax);
   if (lr_encode_batch_ok(L, a, LR_PACK_TENSOR) && lr_batch_part_floats(ctx->sms, d_out, d_in) <= kNoAllocPartFloats) {
     if (!f->planes && launch_lr_split_u_all(L, f->U, d_out, d_in, f->rank, 2, split) != cudaSuccess)
       return GIFT_ERR_CUDA;

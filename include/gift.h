@@ -372,8 +372,8 @@ gift_status gift_select_fragile(int L, const unsigned long long *counts, int k, 
                                 int *order, double *scores, int *k_out);
 
 /* Rank-r encode that allocates nothing (the paper has no counterpart; this is a library
- * convenience).  Same result as gift_encode with a LOWRANK factor, E4M3 or E5M2 and
- * per-tensor scaling, but without a caller workspace: for callers that cannot allocate
+ * convenience).  Same result as gift_encode with a LOWRANK factor, GIFT_PREC_FP32, E4M3 or
+ * E5M2 and per-tensor scaling, but without a caller workspace: for callers that cannot allocate
  * device memory at the point where they encode, such as code running inside a gradient or
  * communication hook while the framework's allocator must not grow, or C programs with no
  * allocator of their own.  Its scratch (about 17 MiB) is a fixed array inside the library,

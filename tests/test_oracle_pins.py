@@ -13,9 +13,18 @@ import numpy as np
 import pytest
 import torch
 
-import oracle as O
+import oracle.gift_oracle as oracle_numpy
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# Both statements of the oracle (numpy, and the single-threaded C++ library) answer to every pin.
+@pytest.fixture(params=["numpy", "cpp"], scope="module")
+def O(request):
+    if request.param == "numpy":
+        return oracle_numpy
+    import oracle.cpp as oracle_cpp
+    return oracle_cpp
 
 
 # ---------------------------------------------------------------------------------------
@@ -70,14 +79,15 @@ def probe_values(fmt_fields, maxval):
 
 
 FIELDS = {"e4m3": ((4, 3, 7), 448.0, 8), "e5m2": ((5, 2, 15), 57344.0, 8), "e2m1": ((2, 1, 1), 6.0, 4)}
-OFMT = {"e4m3": O.E4M3, "e5m2": O.E5M2, "e2m1": O.E2M1}
+def OFMT(O):
+    return {"e4m3": O.E4M3, "e5m2": O.E5M2, "e2m1": O.E2M1}
 
 
 # ---------------------------------------------------------------------------------------
 # number formats
 # ---------------------------------------------------------------------------------------
 
-def test_format_constants_from_pages():
+def test_format_constants_from_pages(O):
     # GIFT reading notes, prerequisites, "What FP8 is": E4M3 max ~448, E5M2 max ~57344,
     # 2^3 or 2^2 mantissa levels per octave.
     assert O.decode([O.E4M3.max_code], O.E4M3)[0] == 448.0
@@ -95,29 +105,29 @@ def test_format_constants_from_pages():
 
 
 @pytest.mark.parametrize("name,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
-def test_decode_matches_torch_float8(name, tdt):
+def test_decode_matches_torch_float8(O, name, tdt):
     codes = np.arange(256, dtype=np.uint8)
     ref = torch.from_numpy(codes).view(tdt).to(torch.float64).numpy()
-    got = O.decode(codes, OFMT[name])
+    got = O.decode(codes, OFMT(O)[name])
     np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
     ok = ~np.isnan(ref)
     np.testing.assert_array_equal(got[ok], ref[ok])
 
 
 @pytest.mark.parametrize("name", ["e4m3", "e5m2", "e2m1"])
-def test_encode_matches_brute_force(name):
+def test_encode_matches_brute_force(O, name):
     fields, maxval, nbits = FIELDS[name]
     y = probe_values(fields, maxval)
-    np.testing.assert_array_equal(O.encode(y, OFMT[name]), brute_encode(y, fields, maxval, nbits))
+    np.testing.assert_array_equal(O.encode(y, OFMT(O)[name]), brute_encode(y, fields, maxval, nbits))
 
 
 @pytest.mark.parametrize("name,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
-def test_encode_matches_torch_in_range(name, tdt):
+def test_encode_matches_torch_in_range(O, name, tdt):
     fields, maxval, _ = FIELDS[name]
     y = probe_values(fields, maxval)
     y = y[np.abs(y) < maxval]
     ref = torch.from_numpy(y).to(tdt).view(torch.uint8).numpy()
-    np.testing.assert_array_equal(O.encode(y, OFMT[name]), ref)
+    np.testing.assert_array_equal(O.encode(y, OFMT(O)[name]), ref)
 
 
 # ---------------------------------------------------------------------------------------
@@ -125,22 +135,22 @@ def test_encode_matches_torch_in_range(name, tdt):
 # ---------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["e4m3", "e5m2"])
-def test_quantize_8x8_brute_force(name):
+def test_quantize_8x8_brute_force(O, name):
     # the scale rule s = amax/FP8_MAX (prerequisites, "What FP8 is"); codes by exhaustive search
     fields, maxval, nbits = FIELDS[name]
     rng = np.random.default_rng(3)
     x = (rng.standard_normal((8, 8)) * np.exp(rng.uniform(-6, 3, (8, 8)))).astype(np.float32)
-    codes, s, amax = O.quantize_tensor(x, OFMT[name])
+    codes, s, amax = O.quantize_tensor(x, OFMT(O)[name])
     assert amax == np.max(np.abs(x))
     assert s == np.float32(amax) / np.float32(maxval)
     m = np.float32(maxval) / np.float32(amax)
     y = (x * m).astype(np.float32)
     np.testing.assert_array_equal(codes, brute_encode(y.ravel(), fields, maxval, nbits).reshape(8, 8))
     # the largest element lands on the format's largest value
-    assert (int(codes.ravel()[np.argmax(np.abs(x))]) & 0x7F) == OFMT[name].max_code
+    assert (int(codes.ravel()[np.argmax(np.abs(x))]) & 0x7F) == OFMT(O)[name].max_code
 
 
-def test_dequant_error_bound():
+def test_dequant_error_bound(O):
     rng = np.random.default_rng(4)
     x = rng.standard_normal(4096).astype(np.float32) * 3
     codes, s, _ = O.quantize_tensor(x, O.E4M3)
@@ -151,7 +161,7 @@ def test_dequant_error_bound():
     assert np.all(np.abs(xh - x) <= bound)
 
 
-def test_zero_and_tiny_amax():
+def test_zero_and_tiny_amax(O):
     codes, s, amax = O.quantize_tensor(np.array([0.0, -0.0, 0.0], np.float32), O.E4M3)
     assert s == 0 and amax == 0 and list(codes) == [0, 0x80, 0]
     x = np.array([1e-40, -1e-40, 0.0], np.float32)   # subnormal amax: m overflows, clamped
@@ -159,14 +169,14 @@ def test_zero_and_tiny_amax():
     assert np.all(np.isfinite(O.decode(codes, O.E4M3)))
 
 
-def test_nonfinite_raises():
+def test_nonfinite_raises(O):
     with pytest.raises(O.NonFinite):
         O.quantize_tensor(np.array([1.0, np.nan], np.float32), O.E4M3)
     with pytest.raises(O.NonFinite):
         O.quantize_tensor(np.array([1.0, np.inf], np.float32), O.E5M2)
 
 
-def test_block128_tiles_and_edges():
+def test_block128_tiles_and_edges(O):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((300, 200)).astype(np.float32)
     x[130:140, 150:160] *= 100
@@ -181,7 +191,7 @@ def test_block128_tiles_and_edges():
             assert scales[i, j] == s
 
 
-def test_nvfp4_brute_force():
+def test_nvfp4_brute_force(O):
     rng = np.random.default_rng(6)
     x = (rng.standard_normal((5, 64)) * np.exp(rng.uniform(-4, 4, (5, 1)))).astype(np.float32)
     packed, bs, st, at = O.quantize_nvfp4(x)
@@ -216,7 +226,7 @@ def test_nvfp4_brute_force():
 # replica reduce (eq. (1): g_bar = (1/R) sum_r g^(r))
 # ---------------------------------------------------------------------------------------
 
-def test_replica_reduce_exact_mean():
+def test_replica_reduce_exact_mean(O):
     # codes and power-of-two scales chosen so that every partial sum is exact: the
     # result must then equal the mathematical mean of eq. (1)
     rng = np.random.default_rng(8)
@@ -232,7 +242,7 @@ def test_replica_reduce_exact_mean():
     np.testing.assert_array_equal(out, np.array([float(e / R) for e in exact], np.float32))
 
 
-def test_replica_reduce_single_is_dequant():
+def test_replica_reduce_single_is_dequant(O):
     x = np.random.default_rng(9).standard_normal((7, 33)).astype(np.float32)
     q = O.quantize(x, "e5m2")
     np.testing.assert_array_equal(O.replica_reduce([q], "e5m2"), O.dequantize_any(q, "e5m2"))
@@ -242,7 +252,7 @@ def test_replica_reduce_single_is_dequant():
 # boundary-hit profiler (three simplifications, simplification 3)
 # ---------------------------------------------------------------------------------------
 
-def test_boundary_hits_hand_example():
+def test_boundary_hits_hand_example(O):
     # amax = 1 -> m = 448: 1 -> 448 (upper), -1 -> -448 (upper), 0.5 -> 224,
     # 1e-6 -> 4.48e-4 < 2^-10 flushes to zero (lower), 0 is not counted, 3e-4 -> 0.1344
     x = np.array([1.0, -1.0, 0.5, 1e-6, 0.0, 3e-4], np.float32)
@@ -251,7 +261,7 @@ def test_boundary_hits_hand_example():
     assert O.boundary_hits(x, "e5m2") == (2, 0, 6)
 
 
-def test_boundary_hits_brute_force():
+def test_boundary_hits_brute_force(O):
     rng = np.random.default_rng(10)
     x = (rng.standard_t(3, (40, 50)) * np.exp(2 * rng.standard_normal(50))).astype(np.float32)
     x[0, :5] = 0
@@ -260,42 +270,42 @@ def test_boundary_hits_brute_force():
         amax = np.max(np.abs(x))
         m = np.float32(maxval) / np.float32(amax)
         codes = brute_encode((x * m).astype(np.float32).ravel(), fields, maxval, nbits)
-        vals = np.abs(O.decode(codes, OFMT[name]))
+        vals = np.abs(O.decode(codes, OFMT(O)[name]))
         up = sum(1 for v in vals if v == maxval)
         lo = sum(1 for v, xx in zip(vals, x.ravel()) if v == 0 and xx != 0)
         assert O.boundary_hits(x, name) == (up, lo, x.size)
 
 
-def test_block1d_single_block_is_per_tensor():
+def test_block1d_single_block_is_per_tensor(O):
     x = np.random.default_rng(40).standard_normal((20, 25)).astype(np.float32)   # 500 elements
     for name in ("e4m3", "e5m2"):
-        c, s, a = O.quantize_block1d(x, OFMT[name])
-        ct, st, at = O.quantize_tensor(x, OFMT[name])
+        c, s, a = O.quantize_block1d(x, OFMT(O)[name])
+        ct, st, at = O.quantize_tensor(x, OFMT(O)[name])
         np.testing.assert_array_equal(c, ct)
         assert s.shape == (1,) and s[0] == st and a[0] == at
 
 
-def test_block1d_power_of_two_copies():
+def test_block1d_power_of_two_copies(O):
     # blocks that are power-of-two multiples of one block: identical codes, scales in the
     # same ratios exactly; a block boundary off by any amount mixes scales and breaks this
     base = np.random.default_rng(41).standard_normal(512).astype(np.float32)
     ks = [-3, 0, 2, 5]
     x = np.stack([base * np.float32(2.0 ** k) for k in ks]).reshape(8, 256)
     for name in ("e4m3", "e5m2"):
-        c, s, _ = O.quantize_block1d(x, OFMT[name])
+        c, s, _ = O.quantize_block1d(x, OFMT(O)[name])
         blocks = c.reshape(4, 512)
         for i in range(4):
             np.testing.assert_array_equal(blocks[i], blocks[1])
             assert s[i] == s[1] * np.float32(2.0 ** ks[i])
 
 
-def test_block1d_ragged_tail_and_roundtrip():
+def test_block1d_ragged_tail_and_roundtrip(O):
     rng = np.random.default_rng(42)
     x = rng.standard_normal((10, 100)).astype(np.float32)      # 1000 elements: 512 + 488
     x.ravel()[900] = 1000.0                                     # an outlier in the short block
     q = O.quantize(x, "e4m3", "block512")
     assert q["scales"].shape == (2,)
-    ct, st, _ = O.quantize_tensor(x.ravel()[:512], OFMT["e4m3"])
+    ct, st, _ = O.quantize_tensor(x.ravel()[:512], OFMT(O)["e4m3"])
     np.testing.assert_array_equal(q["codes"].ravel()[:512], ct)
     assert q["scales"][0] == st and q["scales"][1] == np.float32(1000.0) / np.float32(448.0)
     # round trip within half a code step of the scaled value, plus the subnormal step
@@ -307,7 +317,7 @@ def test_block1d_ragged_tail_and_roundtrip():
 
 @pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "tensor"), ("e4m3", "block128"),
                                          ("e5m2", "block512"), ("nvfp4", "tensor")])
-def test_quantisers_are_power_of_two_equivariant(fmt, scaling):
+def test_quantisers_are_power_of_two_equivariant(O, fmt, scaling):
     # scaling a tensor by 2^k scales amax, s and every block amax by 2^k exactly and leaves
     # every scaled value x * m unchanged: the codes must not move and the stored scales must
     # scale exactly (the NVFP4 block scales are ratios of amaxes and must not move either)
@@ -324,7 +334,7 @@ def test_quantisers_are_power_of_two_equivariant(fmt, scaling):
             np.testing.assert_array_equal(qk["scales"], q0["scales"] * np.float32(2.0 ** k))
 
 
-def test_transforms_are_homogeneous_in_the_factor():
+def test_transforms_are_homogeneous_in_the_factor(O):
     # A -> c A: T_A -> c^-1/2 T_A (whitening scales by c^-1/2, map-back by c^1/2), for the
     # sigma-completed rank-r factor and for the Cholesky factor (L -> c^1/2 L)
     rng = np.random.default_rng(44)
@@ -343,7 +353,7 @@ def test_transforms_are_homogeneous_in_the_factor():
     np.testing.assert_allclose(xfc.unwhiten(X), xf.unwhiten(X) * 3.0, rtol=1e-12, atol=1e-14)
 
 
-def test_select_fragile_ties():
+def test_select_fragile_ties(O):
     assert O.select_fragile([0.1, 0.3, 0.3, 0.05, 0.2], 3) == [1, 2, 4]
 
 
@@ -356,13 +366,13 @@ def _spd(n, seed, cond=1e3):
     return synth.spd_matrix(n, cond, seed).numpy()
 
 
-def test_kfac_factor_matches_outer_products():
+def test_kfac_factor_matches_outer_products(O):
     a = np.random.default_rng(11).standard_normal((9, 4))
     A = sum(np.outer(r, r) for r in a) / 9
     np.testing.assert_allclose(O.kfac_factor(a), A, rtol=1e-14, atol=1e-15)
 
 
-def test_global_factor_is_the_stacked_factor():
+def test_global_factor_is_the_stacked_factor(O):
     # the replica-averaged factor (1/R) sum_r a_r^T a_r / T, for replicas of equal T, is the
     # factor of the replicas' activations stacked into one batch of R T rows
     rng = np.random.default_rng(12)
@@ -371,7 +381,7 @@ def test_global_factor_is_the_stacked_factor():
     np.testing.assert_allclose(O.kfac_factor(np.concatenate(acts)), mean, rtol=1e-13, atol=1e-14)
 
 
-def test_cholesky_vs_lapack_and_identities():
+def test_cholesky_vs_lapack_and_identities(O):
     A = _spd(24, 1)
     L = O.cholesky(A)
     np.testing.assert_allclose(L, np.linalg.cholesky(A), rtol=1e-10, atol=1e-12)
@@ -383,7 +393,7 @@ def test_cholesky_vs_lapack_and_identities():
         O.cholesky(np.array([[1.0, 2.0], [2.0, 1.0]]))
 
 
-def test_triangular_solves_vs_scipy():
+def test_triangular_solves_vs_scipy(O):
     import scipy.linalg as sl
     rng = np.random.default_rng(12)
     LA = O.cholesky(_spd(10, 2))
@@ -396,7 +406,7 @@ def test_triangular_solves_vs_scipy():
                                rtol=1e-10, atol=1e-12)
 
 
-def test_eq9_kfac_norm_equals_whitened_frobenius():
+def test_eq9_kfac_norm_equals_whitened_frobenius(O):
     # ||dW||^2_F_W = vec(dW)^T (A (x) G) vec(dW) = ||L_G^T dW L_A||_F^2 (eqs. (5), (9)), vec = column stacking
     rng = np.random.default_rng(13)
     A, G = _spd(4, 4, 50), _spd(3, 5, 20)
@@ -408,7 +418,7 @@ def test_eq9_kfac_norm_equals_whitened_frobenius():
     assert np.isclose(lhs, np.sum((LG.T @ dW @ LA) ** 2), rtol=1e-12)
 
 
-def test_eq12_two_sided_transform_kronecker_form():
+def test_eq12_two_sided_transform_kronecker_form(O):
     # vec(W~) = (L_A^-1 (x) L_G^-1) vec(W_g)  (eq. (12)); catches transposed or swapped factors
     rng = np.random.default_rng(14)
     A, G = _spd(5, 6, 30), _spd(4, 7, 30)
@@ -425,7 +435,7 @@ def test_eq12_two_sided_transform_kronecker_form():
                                rtol=1e-10, atol=1e-12)
 
 
-def test_whitening_with_given_inverses_matches_solves():
+def test_whitening_with_given_inverses_matches_solves(O):
     # eq. (11) written with L^-1 (factor carries the inverses) equals the triangular solves
     rng = np.random.default_rng(26)
     LA, LG = O.cholesky(_spd(30, 27, 1e4)), O.cholesky(_spd(7, 28, 1e2))
@@ -437,7 +447,7 @@ def test_whitening_with_given_inverses_matches_solves():
 
 
 @pytest.mark.parametrize("kind", ["identity", "lowrank", "chol_input", "chol_two_sided"])
-def test_eq14_map_back_inverts_eq11(kind):
+def test_eq14_map_back_inverts_eq11(O, kind):
     # with a lossless format the map back is exact (common confusions: lossless GIFT = baseline)
     rng = np.random.default_rng(15)
     d_out, d_in = 6, 40
@@ -453,7 +463,7 @@ def test_eq14_map_back_inverts_eq11(kind):
 # low-rank factor (simplification 2, eq. (17)) and its transform
 # ---------------------------------------------------------------------------------------
 
-def test_jacobi_vs_lapack_and_2x2():
+def test_jacobi_vs_lapack_and_2x2(O):
     S = np.random.default_rng(16).standard_normal((40, 40))
     S = S + S.T
     w, V = O.jacobi_eigh(S)
@@ -463,7 +473,7 @@ def test_jacobi_vs_lapack_and_2x2():
     np.testing.assert_allclose(V @ np.diag(w) @ V.T, S, atol=1e-11)
 
 
-def test_subspace_iteration_vs_lapack():
+def test_subspace_iteration_vs_lapack(O):
     from fac_whitening_gb300 import synth
     Q = synth.haar_orthogonal(400, 18, "cpu", torch.float64).numpy()
     ev = np.arange(1, 401, dtype=np.float64) ** -1.6
@@ -476,7 +486,7 @@ def test_subspace_iteration_vs_lapack():
     np.testing.assert_allclose(U[:, :32].T @ U[:, :32], np.eye(32), atol=1e-12)
 
 
-def test_lowrank_full_rank_whitens_exactly():
+def test_lowrank_full_rank_whitens_exactly(O):
     # r = d_in: T_A^T A T_A = I, and T_A equals the symmetric A^-1/2 (LAPACK eigh)
     A = _spd(12, 19, 1e3)
     F = O.lowrank_factor_from_A(A, r=12)
@@ -486,7 +496,7 @@ def test_lowrank_full_rank_whitens_exactly():
     np.testing.assert_allclose(T, (V / np.sqrt(w)) @ V.T, atol=1e-9)
 
 
-def test_lowrank_completion_properties():
+def test_lowrank_completion_properties(O):
     from fac_whitening_gb300 import synth
     rng = np.random.default_rng(20)
     a = synth.activations(600, 96, synth.spectrum_power_law(96, 1.0),
@@ -513,7 +523,7 @@ def test_lowrank_completion_properties():
     assert np.isclose(F2.sigma, F.sigma, rtol=1e-10)
 
 
-def test_lowrank_activation_route_large():
+def test_lowrank_activation_route_large(O):
     from fac_whitening_gb300 import synth
     a = synth.activations(1024, 300, synth.spectrum_power_law(300, 1.0),
                           synth.haar_orthogonal(300, 23), 24).numpy()
@@ -523,7 +533,7 @@ def test_lowrank_activation_route_large():
     assert np.isclose(F.sigma, np.mean(ev[32:]), rtol=1e-9)
 
 
-def test_error_feedback_update():
+def test_error_feedback_update(O):
     # Algorithm 1, geometry-aware branch: U~ = U + R; R <- U~ - Dequantize(Q(U~)).
     # deq and U~ are within a factor two of each other (or deq = 0), so the new
     # residual is exact: deq + R_new == U~ bit for bit.
@@ -536,7 +546,7 @@ def test_error_feedback_update():
     np.testing.assert_array_equal((deq + R1).astype(np.float32), Ut)
 
 
-def test_fidelity_closed_forms():
+def test_fidelity_closed_forms(O):
     g = np.array([3.0, -4.0, 0.0, 12.0])
     f = O.fidelity(g, g)
     assert f["rel_l2"] == 0 and np.isclose(f["cos"], 1) and f["max_err"] == 0 and f["mse"] == 0
@@ -550,7 +560,7 @@ def test_fidelity_closed_forms():
 # the worked 2x2 example (golden values printed on the page)
 # ---------------------------------------------------------------------------------------
 
-def test_toy_2x2_golden():
+def test_toy_2x2_golden(O):
     gold = json.load(open(os.path.join(GOLDEN, "toy_2x2.json")))
 
     def tol(entry):

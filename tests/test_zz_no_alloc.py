@@ -5,7 +5,10 @@ example code running inside a gradient or communication hook while the framework
 allocator must not grow, or C callers without an allocator of their own): it keeps its
 scratch in a fixed array inside the library instead of a caller workspace.  This test
 calls it through the C ABI twice in a row (the second call must not see the first
-call's scratch) and compares codes, scale and amax with gift_encode's, bit for bit.
+call's scratch) and compares codes, scale and amax with gift_encode's (FP32 precision), bit
+for bit, on every route the entry point takes: the batched tensor-core encode (the 600M-like
+fc2 shape), the two-launch tensor-core apply (a shape whose row blocks do not fit the batched
+plan), the FP32-SIMT path (d_in not a multiple of 32), and a caller-supplied amax.
 The file is collected last on purpose.
 """
 import ctypes
@@ -32,16 +35,20 @@ def _factor(d_out, d_in, rank, seed):
     g = torch.Generator(device="cpu").manual_seed(seed)
     q, _ = torch.linalg.qr(torch.randn(d_in, rank, generator=g, dtype=torch.float64))
     mu = torch.sort(torch.rand(rank, generator=g, dtype=torch.float64) * 10 + 1, descending=True).values
-    f = G.Factor("lowrank", d_out, d_in, rank, U=q.float().cuda(), mu=mu.float().cuda(),
+    # torch's QR returns a column-major Q; the library takes row-major, contiguous buffers
+    f = G.Factor("lowrank", d_out, d_in, rank, U=q.float().contiguous().cuda(), mu=mu.float().cuda(),
                  sigma=torch.tensor([0.05], device="cuda"))
     return f
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_noalloc_matches_gift_encode_twice(fmt):
+@pytest.mark.parametrize("shape,fmt,shared", [
+    ((1536, 6144), "e4m3", False), ((1536, 6144), "e5m2", False), ((1536, 6144), "e4m3", True),
+    ((4096, 4096), "e4m3", False), ((256, 1000), "e5m2", False), ((256, 1000), "e4m3", True)],
+    ids=["600m-e4m3", "600m-e5m2", "600m-amax_in", "4096sq-e4m3", "simt-e5m2", "simt-amax_in"])
+def test_noalloc_matches_gift_encode_twice(shape, fmt, shared):
     ctx = G.Context(torch.cuda.current_device())
     fn = _noalloc_fn()
-    d_out, d_in = 1536, 6144
+    d_out, d_in = shape
     f = _factor(d_out, d_in, 32, 3)
     fs = f.c_struct()
     stream = torch.cuda.current_stream().cuda_stream
@@ -54,12 +61,16 @@ def test_noalloc_matches_gift_encode_twice(fmt):
         c_ref = torch.empty(d_out * d_in, dtype=torch.uint8, device="cuda")
         s_ref = torch.empty(1, dtype=torch.float32, device="cuda")
         a_ref = torch.empty(1, dtype=torch.float32, device="cuda")
-        G.gift_encode(ctx, f, W, fmt, "tensor", c_ref, s_ref, amax_out=a_ref, ws=ws)
+        # a caller amax (the shared scale of the Euclidean path), below the tensor's own on the
+        # first call (codes saturate) and above it on the second
+        a_in = torch.tensor([3.0 if call == 0 else 0.25], device="cuda") if shared else None
+        G.gift_encode(ctx, f, W, fmt, "tensor", c_ref, s_ref, amax_in=a_in, amax_out=a_ref, ws=ws)
         c = torch.empty_like(c_ref)
         s = torch.empty_like(s_ref)
         a = torch.empty_like(a_ref)
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        rc = fn(ctx.handle, ctypes.byref(fs), W.data_ptr(), d_out, d_in, G.FMT[fmt], None, c.data_ptr(),
+        rc = fn(ctx.handle, ctypes.byref(fs), W.data_ptr(), d_out, d_in, G.FMT[fmt],
+                None if a_in is None else a_in.data_ptr(), c.data_ptr(),
                 s.data_ptr(), a.data_ptr(), st.data_ptr(), stream)
         assert rc == G.OK
         torch.cuda.synchronize()
