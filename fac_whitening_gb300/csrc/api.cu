@@ -47,6 +47,7 @@ struct CodecWs {
   float *split = nullptr;  // LOWRANK: tensor-core operand planes and counters (kernels.cuh)
   float *bpart = nullptr;  // LOWRANK, batched encode: kBatchWs x lr_batch_part_floats
   uint16_t *bplanes = nullptr;   // LOWRANK, batched encode: kBatchWs x 2 x d_out rows of 64 BF16
+  void *gplanes = nullptr;       // CHOL: BF16 term planes of the tensor-core GEMMs' operands
   int nsplit = 0;
   size_t bytes = 0;
 };
@@ -71,6 +72,12 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
     if (op == GIFT_OP_DECODE || kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED)
       w.xbuf = c.take<float>(n);
     if (kind == GIFT_XF_CHOL_TWO_SIDED) w.tbuf = c.take<float>(n);
+    if (kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED) {
+      // X L^-T (or X L^T) has K = d_in; the left factor's product K = d_out
+      size_t g = gemm_tc_ws_bytes(d_out, d_in, d_in, 3);
+      if (kind == GIFT_XF_CHOL_TWO_SIDED) g = std::max(g, gemm_tc_ws_bytes(d_out, d_in, d_out, 3));
+      w.gplanes = c.take<uint8_t>(g);
+    }
   }
   w.bytes = c.off;
   return w;
@@ -171,43 +178,48 @@ gift_status check_factor(const gift_factor *f, int d_out, int d_in) {
 
 gift_xform kind_of(const gift_factor *f) { return f ? f->kind : GIFT_XF_IDENTITY; }
 
-// Full-rank transforms as GEMMs with the explicit inverses of the factor.
-cudaError_t chol_whiten(const Launch &L, const gift_factor *f, const float *W, int d_out, int d_in,
-                        const CodecWs &w) {
-  const float *src = W;
-  if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
-    GemmArgs g{};
-    g.A = f->LGinv; g.B = W; g.C = w.tbuf;
-    g.M = d_out; g.N = d_in; g.K = d_out; g.lda = d_out; g.ldb = d_in; g.ldc = d_in;
-    g.a_lower = true; g.alpha = 1.0f;
-    cudaError_t e = launch_sgemm(L, g);
-    if (e != cudaSuccess) return e;
-    src = w.tbuf;
-  }
-  GemmArgs g{};
-  g.A = src; g.B = f->LAinv; g.C = w.xbuf;
-  g.M = d_out; g.N = d_in; g.K = d_in; g.lda = d_in; g.ldb = d_in; g.ldc = d_in;
-  g.transB = true; g.b_lower_t = true; g.alpha = 1.0f;
+// One product of a full-rank transform: on the tensor cores with exact BF16 operand splits
+// (three terms and six products at FP32 precision, two terms and three products at TC
+// precision), or FP32 SIMT where the tensor-core path does not apply.
+cudaError_t chol_gemm(const Launch &L, const GemmArgs &g, const CodecWs &w, gift_precision prec) {
+  if (gemm_tc_ok(g, w.gplanes)) return launch_gemm_tc(L, g, prec == GIFT_PREC_TC ? 2 : 3, w.gplanes);
   return launch_sgemm(L, g);
 }
 
-cudaError_t chol_unwhiten(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, float *out,
-                          const CodecWs &w) {
-  const float *src = X;
-  if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
-    GemmArgs g{};
-    g.A = f->LG; g.B = X; g.C = w.tbuf;
-    g.M = d_out; g.N = d_in; g.K = d_out; g.lda = d_out; g.ldb = d_in; g.ldc = d_in;
-    g.a_lower = true; g.alpha = 1.0f;
-    cudaError_t e = launch_sgemm(L, g);
-    if (e != cudaSuccess) return e;
-    src = w.tbuf;
-  }
+// Full-rank transforms as GEMMs with the explicit inverses of the factor: W~ = L_G^-1 W L_A^-T
+// ([notes] core idea step 3, eq. (11)) or W L_A^-T (simplification 1, eq. (16)).  The two-sided
+// form takes W L_A^-T first, then L_G^-1 of it.
+cudaError_t chol_whiten(const Launch &L, const gift_factor *f, const float *W, int d_out, int d_in,
+                        const CodecWs &w, gift_precision prec) {
+  const bool two = f->kind == GIFT_XF_CHOL_TWO_SIDED;
   GemmArgs g{};
-  g.A = src; g.B = f->LA; g.C = out;
+  g.A = W; g.B = f->LAinv; g.C = two ? w.tbuf : w.xbuf;
   g.M = d_out; g.N = d_in; g.K = d_in; g.lda = d_in; g.ldb = d_in; g.ldc = d_in;
   g.transB = true; g.b_lower_t = true; g.alpha = 1.0f;
-  return launch_sgemm(L, g);
+  cudaError_t e = chol_gemm(L, g, w, prec);
+  if (e != cudaSuccess || !two) return e;
+  GemmArgs h{};
+  h.A = f->LGinv; h.B = w.tbuf; h.C = w.xbuf;
+  h.M = d_out; h.N = d_in; h.K = d_out; h.lda = d_out; h.ldb = d_in; h.ldc = d_in;
+  h.a_lower = true; h.alpha = 1.0f;
+  return chol_gemm(L, h, w, prec);
+}
+
+// The map back ([notes] eq. (14)): W^ = L_G X L_A^T, or X L_A^T for the input side only.
+cudaError_t chol_unwhiten(const Launch &L, const gift_factor *f, const float *X, int d_out, int d_in, float *out,
+                          const CodecWs &w, gift_precision prec) {
+  const bool two = f->kind == GIFT_XF_CHOL_TWO_SIDED;
+  GemmArgs g{};
+  g.A = X; g.B = f->LA; g.C = two ? w.tbuf : out;
+  g.M = d_out; g.N = d_in; g.K = d_in; g.lda = d_in; g.ldb = d_in; g.ldc = d_in;
+  g.transB = true; g.b_lower_t = true; g.alpha = 1.0f;
+  cudaError_t e = chol_gemm(L, g, w, prec);
+  if (e != cudaSuccess || !two) return e;
+  GemmArgs h{};
+  h.A = f->LG; h.B = w.tbuf; h.C = out;
+  h.M = d_out; h.N = d_in; h.K = d_out; h.lda = d_out; h.ldb = d_in; h.ldc = d_in;
+  h.a_lower = true; h.alpha = 1.0f;
+  return chol_gemm(L, h, w, prec);
 }
 
 LrApply lr_args(const gift_factor *f, const float *X, int d_out, int d_in, const CodecWs &w, bool inverse,
@@ -557,7 +569,7 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   }
   const float *src = W;
   if (kind != GIFT_XF_IDENTITY) {
-    CK(chol_whiten(L, f, W, d_out, d_in, w));
+    CK(chol_whiten(L, f, W, d_out, d_in, w, prec));
     src = w.xbuf;
   }
   if (block) CK(launch_block128(L, fmt, 1, src, const_cast<float *>(residual), d_out, d_in, nullptr, nullptr,
@@ -636,7 +648,7 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
 
   const float *src = W;
   if (kind != GIFT_XF_IDENTITY) {
-    CK(chol_whiten(L, f, W, d_out, d_in, w));
+    CK(chol_whiten(L, f, W, d_out, d_in, w, prec));
     src = w.xbuf;
   }
   if (fmt == GIFT_FMT_F32) {
@@ -899,7 +911,7 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
     a.out = W_out;
     CK(launch_lr_apply(L, LR_STORE, GIFT_FMT_F32, a));
   } else {
-    CK(chol_unwhiten(L, f, X, d_out, d_in, W_out, w));
+    CK(chol_unwhiten(L, f, X, d_out, d_in, W_out, w, prec));
   }
   return GIFT_OK;
 }

@@ -196,6 +196,19 @@ struct GemmArgs {
   float alpha;
 };
 cudaError_t launch_sgemm(const Launch &L, const GemmArgs &g);
+// gemm_tc.cu: the same product on tcgen05 with the operands split exactly into nt BF16 term
+// planes (nt = 3: six products, FP32 precision; nt = 2: three products) in ws
+// (gemm_tc_ws_bytes(M, N, K, nt) bytes, 16-byte aligned).  FP32 operands, no transA.
+bool gemm_tc_ok(const GemmArgs &g, const void *ws);
+size_t gemm_tc_ws_bytes(int M, int N, int K, int nterms);
+size_t gemm_tc_plane_bytes(int rows, int K, int nterms);
+cudaError_t launch_gemm_tc(const Launch &L, const GemmArgs &g, int nt, void *ws);
+// The planes alone (rows x K, or the transpose of a K x rows source), and the product of two
+// plane sets C = alpha A B^T; a_lower / b_lower: row i of A (row j of B) is zero beyond k = i (j).
+cudaError_t launch_split_planes(const Launch &L, const float *src, int rows, int K, int ld, bool transpose, int nt,
+                                uint16_t *planes);
+cudaError_t launch_gemm_planes(const Launch &L, const uint16_t *pa, const uint16_t *pb, int M, int N, int K, int nt,
+                               bool a_lower, bool b_lower, float alpha, float *C, int ldc);
 cudaError_t launch_sgemm_splitk(const Launch &L, const GemmArgs &g, float *parts, int splits);
 size_t sgemm_splitk_parts(int M, int ldc, int splits);
 // C = alpha * op(A) op(B) + beta * C in FP64 with float or double operands, split-K slices

@@ -44,15 +44,23 @@ def test_c2_cholesky_factors_full_size(c2):
     f, st = run_factor("chol_two_sided", a.to(DEV), spec.d_out, delta=delta.to(DEV))
     assert st == 0
     for Lt, Lit, x in ((f.LA, f.LAinv, a), (f.LG, f.LGinv, delta)):
-        A = O.kfac_factor(x.double().numpy())
+        d = x.shape[1]
         L, Li = Lt.cpu().double().numpy(), Lit.cpu().double().numpy()
         assert np.all(np.triu(L, 1) == 0) and np.all(np.triu(Li, 1) == 0)
-        # A is formed on the device by FP32 accumulation over T = 8192 tokens: about sqrt(T) u
-        # = 90 x 6e-8 = 5e-6 relative (u the FP32 unit roundoff); L itself is exact to FP32
+        # The factor of the exact A: A is formed on the device by FP32 accumulation over
+        # T = 8192 tokens, about sqrt(T) u = 90 x 6e-8 = 5e-6 relative (u the FP32 unit
+        # roundoff), and L L^T reproduces it to that.
+        A = O.kfac_factor(x.double().numpy())
         assert rel_fro(L @ L.T, A) <= 1e-5
-        Lo = O.cholesky(A)
-        assert rel_fro(L, Lo) <= 1e-4
-        assert rel_fro(Li, O.lower_inverse(Lo)) <= 1e-3
+        # The factorisation itself, against the oracle's Cholesky of the device's own A (the
+        # same FP32 K-FAC product gift_kfac_factor returns): FP64 on both sides, so the only
+        # difference is L and L^-1 rounded to FP32.
+        Ag = torch.empty(d, d, device=DEV)
+        G.gift_kfac_factor(ctx(), x.to(DEV), Ag, prec="fp32", status=status())
+        torch.cuda.synchronize()
+        Lo = O.cholesky(Ag.cpu().double().numpy())
+        assert rel_fro(L, Lo) <= 1e-6
+        assert rel_fro(Li, O.lower_inverse(Lo)) <= 1e-6
 
 
 @pytest.mark.parametrize("kind", ["chol_input", "chol_two_sided"])
