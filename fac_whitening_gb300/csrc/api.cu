@@ -34,7 +34,9 @@ struct Carve {
 };
 
 bool valid_fmt(gift_format f) { return f >= GIFT_FMT_F32 && f <= GIFT_FMT_NVFP4; }
-bool valid_scaling(gift_scaling s) { return s == GIFT_SCALE_TENSOR || s == GIFT_SCALE_BLOCK128; }
+bool valid_scaling(gift_scaling s) {
+  return s == GIFT_SCALE_TENSOR || s == GIFT_SCALE_BLOCK128 || s == GIFT_SCALE_BLOCK512;
+}
 bool valid_kind(gift_xform k) { return k >= GIFT_XF_IDENTITY && k <= GIFT_XF_CHOL_TWO_SIDED; }
 
 // ---- codec workspace (encode / amax / decode) -----------------------------------------
@@ -158,6 +160,7 @@ Launch mk(const gift_ctx *ctx, int *st, cudaStream_t s) {
   L.stream = s;
   L.sms = ctx->sms;
   L.status = st;
+  L.barrier_wait = ctx->barrier_wait;
   return L;
 }
 
@@ -271,6 +274,7 @@ gift_status gift_create(gift_ctx **ctx, int device) {
   c->device = device;
   c->sms = sms;
   c->subspace_iters = 10;
+  c->barrier_wait = kDefaultBarrierWait;
   *ctx = c;
   return GIFT_OK;
 }
@@ -282,6 +286,11 @@ gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value) {
   if (opt == GIFT_OPT_SUBSPACE_ITERS) {
     if (value < 1 || value > 64) return GIFT_ERR_INVALID_ARG;
     ctx->subspace_iters = (int)value;
+    return GIFT_OK;
+  }
+  if (opt == GIFT_OPT_BARRIER_WAIT) {
+    if (value < 0 || value > 20000000000LL) return GIFT_ERR_INVALID_ARG;
+    ctx->barrier_wait = value;
     return GIFT_OK;
   }
   return GIFT_ERR_INVALID_ARG;
@@ -334,9 +343,9 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
       break;
     default:
       *code_bytes = n;
-      *scale_count = (scaling == GIFT_SCALE_TENSOR)
-                         ? 1
-                         : (size_t)((d_out + kBlock - 1) / kBlock) * ((d_in + kBlock - 1) / kBlock);
+      *scale_count = (scaling == GIFT_SCALE_TENSOR)     ? 1
+                     : (scaling == GIFT_SCALE_BLOCK512) ? (n + kBlock1d - 1) / kBlock1d
+                                                        : (size_t)((d_out + kBlock - 1) / kBlock) * ((d_in + kBlock - 1) / kBlock);
   }
   return GIFT_OK;
 }
@@ -487,7 +496,11 @@ static gift_status codec_common_checks(gift_ctx *ctx, const gift_factor *f, cons
   if (!ctx || !W || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
   if (!valid_fmt(fmt) || !valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
   if (fmt == GIFT_FMT_NVFP4 && d_in % kNvGroup) return GIFT_ERR_INVALID_ARG;
-  return check_factor(f, d_out, d_in);
+  const gift_status fs = check_factor(f, d_out, d_in);
+  if (fs != GIFT_OK) return fs;
+  if (scaling == GIFT_SCALE_BLOCK512 && fmt != GIFT_FMT_NVFP4 && fmt != GIFT_FMT_F32 && kind_of(f) == GIFT_XF_LOWRANK)
+    return GIFT_ERR_UNSUPPORTED;
+  return GIFT_OK;
 }
 
 static gift_status encode_checks(gift_ctx *ctx, const gift_factor *f, const float *W, int d_out, int d_in,
@@ -549,6 +562,7 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
   const Launch L = mk(ctx, d_status, stream);
   const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
+  const bool b512 = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK512);
   const size_t n = (size_t)d_out * d_in;
   if (kind == GIFT_XF_LOWRANK) {
     if (!block && !residual) {
@@ -574,6 +588,8 @@ gift_status gift_amax(gift_ctx *ctx, const gift_factor *f, const float *W, int d
   }
   if (block) CK(launch_block128(L, fmt, 1, src, const_cast<float *>(residual), d_out, d_in, nullptr, nullptr,
                                 nullptr, amax_accum, nullptr, nullptr));
+  else if (b512) CK(launch_block512(L, fmt, 1, src, const_cast<float *>(residual), n, nullptr, nullptr, nullptr,
+                                    amax_accum, nullptr, nullptr));
   else CK(launch_amax(L, src, residual, n, amax_accum));
   return GIFT_OK;
 }
@@ -660,6 +676,11 @@ gift_status gift_encode(gift_ctx *ctx, const gift_factor *f, const float *W, int
                        transformed_out, nullptr));
     return GIFT_OK;
   }
+  if (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK512) {
+    CK(launch_block512(L, fmt, 0, src, residual, n, amax_in, c8, static_cast<float *>(scales), amax_out,
+                       transformed_out, nullptr));
+    return GIFT_OK;
+  }
   const float *amax = amax_in;
   if (!amax) {
     CK(cudaMemsetAsync(w.amax, 0, sizeof(float), stream));
@@ -692,7 +713,7 @@ gift_status gift_encode_replicas(gift_ctx *ctx, const gift_factor *f, int R, con
   }
   const gift_xform kind = kind_of(f);
   const Launch L = mk(ctx, d_status, stream);
-  if (kind == GIFT_XF_LOWRANK && fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128)) {
+  if (kind == GIFT_XF_LOWRANK && fmt != GIFT_FMT_F32 && !(fmt != GIFT_FMT_NVFP4 && scaling != GIFT_SCALE_TENSOR)) {
     const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_ENCODE, kind, d_out, d_in);
     LrEncodeItem items[kMaxReplicas];
     for (int r = 0; r < R; ++r) {
@@ -812,7 +833,7 @@ gift_status gift_amax_replicas(gift_ctx *ctx, const gift_factor *f, int R, const
   const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, kind, d_out, d_in);
   if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
   const Launch L = mk(ctx, d_status, stream);
-  const bool block = (fmt != GIFT_FMT_NVFP4 && scaling == GIFT_SCALE_BLOCK128);
+  const bool block = (fmt != GIFT_FMT_NVFP4 && scaling != GIFT_SCALE_TENSOR);
   if (!block && kind == GIFT_XF_IDENTITY) {
     MultiArgs m;
     std::memset(&m, 0, sizeof(m));
@@ -925,6 +946,11 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
   const Launch L = mk(ctx, d_status, stream);
   if (scaling == GIFT_SCALE_BLOCK128) {
     CK(launch_block128(L, fmt, 2, W, nullptr, d_out, d_in, nullptr, nullptr, nullptr, nullptr, nullptr, d_counts));
+    return GIFT_OK;
+  }
+  if (scaling == GIFT_SCALE_BLOCK512) {
+    CK(launch_block512(L, fmt, 2, W, nullptr, (size_t)d_out * d_in, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       d_counts));
     return GIFT_OK;
   }
   const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, GIFT_XF_IDENTITY, d_out, d_in);

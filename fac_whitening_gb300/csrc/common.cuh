@@ -20,6 +20,7 @@ constexpr float kE5M2Max = 57344.0f;
 constexpr float kNvfp4TensorDiv = 2688.0f;   // 448 * 6: E4M3 block-scale range x E2M1 range
 constexpr float kF32Max = 3.402823466e38f;
 constexpr int kBlock = 128;                  // edge of a BLOCK128 scale tile
+constexpr int kBlock1d = 512;                // elements of a BLOCK512 scale group
 constexpr int kNvGroup = 16;                 // elements per NVFP4 block scale
 constexpr int kMaxRank = 32;
 constexpr int kMaxReplicas = 64;

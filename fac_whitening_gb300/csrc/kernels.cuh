@@ -8,14 +8,18 @@ struct gift_ctx {
   int device;
   int sms;
   int subspace_iters;
+  long long barrier_wait;   // clock cycles a CTA waits at a streaming grid barrier
 };
 
 namespace gift {
+
+constexpr long long kDefaultBarrierWait = 2000000000LL;   // clock cycles, about a second
 
 struct Launch {
   cudaStream_t stream;
   int sms;       // streaming multiprocessors of the device
   int *status;   // caller's device status word (nullable)
+  long long barrier_wait = kDefaultBarrierWait;   // bounded wait of the streaming grid barriers
 };
 
 struct ReduceArgs {
@@ -41,6 +45,11 @@ cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *
 cudaError_t launch_pack_f32(const Launch &L, const float *x, float *r, size_t n, float *out, float *tout);
 // mode 0: pack, 1: amax only (max-accumulated into amax_out), 2: count boundary hits
 cudaError_t launch_block128(const Launch &L, int fmt, int mode, const float *x, float *r, int d_out, int d_in,
+                            const float *amax_in, uint8_t *codes, float *scales, float *amax_out, float *tout,
+                            unsigned long long *counts);
+// 1-D blocks of 512 consecutive elements; modes as launch_block128 (amax_out of mode 1 is
+// max-accumulated per block)
+cudaError_t launch_block512(const Launch &L, int fmt, int mode, const float *x, float *r, size_t n,
                             const float *amax_in, uint8_t *codes, float *scales, float *amax_out, float *tout,
                             unsigned long long *counts);
 cudaError_t launch_pack_nvfp4(const Launch &L, const float *x, float *r, size_t n, const float *amax,

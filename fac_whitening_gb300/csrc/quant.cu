@@ -243,8 +243,6 @@ __global__ void __launch_bounds__(256) k_pack_tensor_multi(MultiArgs a, int R, s
 // are zero on entry.  The barrier wait is bounded: a CTA that gives up sets
 // GIFT_ERR_TIMEOUT and writes no codes.
 // =====================================================================================
-constexpr long long kSharedWait = 2000000000LL;   // clock cycles, about a second
-
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -253,7 +251,7 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
 
 template <int F>
 __global__ void __launch_bounds__(256) k_encode_shared(MultiArgs a, int R, size_t n4, uint32_t *ws,
-                                                       float *shared_out, int *status) {
+                                                       float *shared_out, long long wait_budget, int *status) {
   __shared__ uint32_t red[8];
   __shared__ uint32_t amax_sh, ok_sh;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -275,7 +273,7 @@ __global__ void __launch_bounds__(256) k_encode_shared(MultiArgs a, int R, size_
     uint32_t ok = 1;
     const long long t0 = clock64();
     while (ld_acquire_gpu(ws + 1) < gridDim.x) {
-      if (clock64() - t0 > kSharedWait) {
+      if (clock64() - t0 > wait_budget) {
         ok = 0;
         set_status(status, GIFT_ERR_TIMEOUT);
         break;
@@ -593,19 +591,148 @@ __global__ void __launch_bounds__(256) k_hits_tensor(const float *__restrict__ x
 }
 
 // =====================================================================================
+// 1-D block scaling: one FP32 scale per kBlock1d = 512 consecutive elements of the row-major
+// tensor, the last block shorter (the per-block Euclidean baseline of the experiments, block
+// size 512).  One warp per block: VEC, lane l holds elements 4(l + 32u) .. +3 (u < 4) as
+// float4, every load and store coalesced; otherwise lane l holds elements l + 32j (j < 16).
+// MODE 0: pack (amax_in per block overrides the block's own); MODE 1: amax only
+// (atomicMax into amax_out[block]); MODE 2: count boundary hits.  Per element the
+// arithmetic is that of the per-tensor pack.
+// =====================================================================================
+template <int F, int MODE, bool VEC, bool RES, bool TOUT>
+__global__ void __launch_bounds__(256) k_block512(const float *__restrict__ x, float *__restrict__ r, size_t n,
+                                                  const float *__restrict__ amax_in, uint8_t *__restrict__ codes,
+                                                  float *__restrict__ scales, float *__restrict__ amax_out,
+                                                  float *__restrict__ tout, unsigned long long *__restrict__ counts,
+                                                  int *status) {
+  const int lane = threadIdx.x & 31;
+  const size_t nb = (n + kBlock1d - 1) / kBlock1d;
+  const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
+  uint32_t up = 0, lo = 0, cnt = 0;
+  for (size_t b = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nb; b += warps) {
+    const size_t e0 = b * kBlock1d;
+    const size_t len = min((size_t)kBlock1d, n - e0);
+    float v[16];
+    uint32_t m = 0;
+    if (VEC) {   // n % 4 == 0, 16-byte aligned x (and r)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const size_t i = 4 * (lane + 32 * u);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < len) {
+          a = *reinterpret_cast<const float4 *>(x + e0 + i);
+          if (RES) a = add4(a, *reinterpret_cast<const float4 *>(r + e0 + i));
+        }
+        v[4 * u] = a.x; v[4 * u + 1] = a.y; v[4 * u + 2] = a.z; v[4 * u + 3] = a.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const size_t i = lane + 32 * j;
+        float a = 0.0f;
+        if (i < len) {
+          a = x[e0 + i];
+          if (RES) a = __fadd_rn(a, r[e0 + i]);
+        }
+        v[j] = a;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = max(m, abs_bits(v[j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (MODE == 1) {
+      if (lane == 0) {
+        atomicMax(reinterpret_cast<uint32_t *>(amax_out) + b, m);
+        if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+      }
+      continue;
+    }
+    float amax = __uint_as_float(m);
+    if (MODE == 0 && amax_in) amax = amax_in[b];
+    const ScalePair sp = scale_pair(amax, fmax_of<F>());
+    if (lane == 0) {
+      if (m >= 0x7F800000u || !(amax <= kF32Max)) set_status(status, GIFT_ERR_NONFINITE);
+      if (MODE == 0) {
+        scales[b] = sp.s;
+        if (amax_out) amax_out[b] = amax;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t c = pack4_fp8<F>(__fmul_rn(v[4 * g], sp.m), __fmul_rn(v[4 * g + 1], sp.m),
+                                      __fmul_rn(v[4 * g + 2], sp.m), __fmul_rn(v[4 * g + 3], sp.m));
+      if (VEC) {
+        const size_t i = 4 * (lane + 32 * g);
+        if (i >= len) continue;
+        if (MODE == 2) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t mag = (c >> (8 * e)) & 0x7Fu;
+            up += (mag == maxcode_of<F>());
+            lo += (mag == 0u && v[4 * g + e] != 0.0f);
+            ++cnt;
+          }
+          continue;
+        }
+        *reinterpret_cast<uint32_t *>(codes + e0 + i) = c;
+        if (TOUT) *reinterpret_cast<float4 *>(tout + e0 + i) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        if (RES) {
+          float4 e;
+          e.x = __fsub_rn(v[4 * g], __fmul_rn(dec_fp8<F>(c & 0xFF), sp.s));
+          e.y = __fsub_rn(v[4 * g + 1], __fmul_rn(dec_fp8<F>((c >> 8) & 0xFF), sp.s));
+          e.z = __fsub_rn(v[4 * g + 2], __fmul_rn(dec_fp8<F>((c >> 16) & 0xFF), sp.s));
+          e.w = __fsub_rn(v[4 * g + 3], __fmul_rn(dec_fp8<F>(c >> 24), sp.s));
+          *reinterpret_cast<float4 *>(r + e0 + i) = e;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * g + e;
+          const size_t i = lane + 32 * j;
+          if (i >= len) continue;
+          const uint32_t ce = (c >> (8 * e)) & 0xFFu;
+          if (MODE == 2) {
+            up += ((ce & 0x7Fu) == maxcode_of<F>());
+            lo += ((ce & 0x7Fu) == 0u && v[j] != 0.0f);
+            ++cnt;
+            continue;
+          }
+          codes[e0 + i] = (uint8_t)ce;
+          if (TOUT) tout[e0 + i] = v[j];
+          if (RES) r[e0 + i] = __fsub_rn(v[j], __fmul_rn(dec_fp8<F>(ce), sp.s));
+        }
+      }
+    }
+  }
+  if (MODE == 2) {
+    up = warp_add_u32(up);
+    lo = warp_add_u32(lo);
+    cnt = warp_add_u32(cnt);
+    if (lane == 0 && cnt) {
+      atomicAdd(counts + 0, (unsigned long long)up);
+      atomicAdd(counts + 1, (unsigned long long)lo);
+      atomicAdd(counts + 2, (unsigned long long)cnt);
+    }
+  }
+}
+
+// =====================================================================================
 // Replica reduce: out = (deq_0 + deq_1 + ... + deq_{R-1}) / R, left to right in FP32.
 // Vector path: 16 elements per thread (one 16-byte code load per replica).
 // =====================================================================================
-template <bool BLOCK>
+// SC: 0 per tensor, 1 per 128 x 128 tile, 2 per 512 consecutive elements
+template <int SC>
 __device__ __forceinline__ float replica_scale(const ReduceArgs &a, int rr, size_t e0, int d_in, int nbc) {
   const float *s = reinterpret_cast<const float *>(a.scales[rr]);
-  if (!BLOCK) return s[0];
+  if (SC == 0) return s[0];
+  if (SC == 2) return s[e0 / kBlock1d];
   const size_t row = e0 / (size_t)d_in;
   const int col = (int)(e0 - row * (size_t)d_in);
   return s[(row / kBlock) * nbc + col / kBlock];
 }
 
-template <int F, bool BLOCK>
+template <int F, int SC>
 __global__ void __launch_bounds__(256) k_reduce_fp8_vec(ReduceArgs a, int R, size_t n, int d_in,
                                                         float *__restrict__ out) {
   const size_t n16 = n >> 4;
@@ -624,7 +751,7 @@ __global__ void __launch_bounds__(256) k_reduce_fp8_vec(ReduceArgs a, int R, siz
       for (int u = 0; u < 8; ++u)
         if (r0 + u < R) {
           cc[u] = __ldcs(reinterpret_cast<const uint4 *>(a.codes[r0 + u]) + i);
-          sc[u] = replica_scale<BLOCK>(a, r0 + u, e0, d_in, nbc);
+          sc[u] = replica_scale<SC>(a, r0 + u, e0, d_in, nbc);
         }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -680,7 +807,7 @@ __global__ void __launch_bounds__(256) k_reduce_nvfp4_vec(ReduceArgs a, int R, s
 
 // Generic scalar path (any alignment, any format); element range [start, n).
 // FMTK: 0 E4M3, 1 E5M2, 2 NVFP4, 3 F32.
-template <int FMTK, bool BLOCK>
+template <int FMTK, int SC>
 __global__ void __launch_bounds__(256) k_reduce_scalar(ReduceArgs a, int R, size_t start, size_t n, int d_in,
                                                        float *__restrict__ out) {
   const int nbc = (d_in + kBlock - 1) / kBlock;
@@ -699,14 +826,7 @@ __global__ void __launch_bounds__(256) k_reduce_scalar(ReduceArgs a, int R, size
         d = nvfp4_deq(c, ev, a.tscales[rr][0]);
       } else {
         const uint8_t c = reinterpret_cast<const uint8_t *>(a.codes[rr])[e];
-        float s;
-        if (BLOCK) {
-          const size_t row = e / (size_t)d_in;
-          const int col = (int)(e - row * (size_t)d_in);
-          s = reinterpret_cast<const float *>(a.scales[rr])[(row / kBlock) * nbc + col / kBlock];
-        } else {
-          s = reinterpret_cast<const float *>(a.scales[rr])[0];
-        }
+        const float s = replica_scale<SC>(a, rr, e, d_in, nbc);
         d = __fmul_rn(FMTK == 0 ? dec_e4m3(c) : dec_e5m2(c), s);
       }
       acc = (rr == 0) ? d : __fadd_rn(acc, d);
@@ -828,7 +948,8 @@ cudaError_t launch_encode_shared(const Launch &L, int fmt, const MultiArgs &a, i
   int args_r = R;
   size_t n4 = n / 4;
   int *st = L.status;
-  void *args[] = {&args_a, &args_r, &n4, &ws, &shared_out, &st};
+  long long budget = L.barrier_wait;
+  void *args[] = {&args_a, &args_r, &n4, &ws, &shared_out, &budget, &st};
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid);
@@ -926,19 +1047,27 @@ cudaError_t launch_hits_tensor(const Launch &L, int fmt, const float *x, size_t 
   return cudaGetLastError();
 }
 
+template <int F, int SC>
+static void reduce_fp8(const Launch &L, const ReduceArgs &a, int R, size_t n, size_t done, int d_in, float *out,
+                       bool vec) {
+  if (vec) k_reduce_fp8_vec<F, SC><<<stream_grid(L, n / 16, 256), 256, 0, L.stream>>>(a, R, n, d_in, out);
+  if (done < n)
+    k_reduce_scalar<F == FMT_E4M3 ? 0 : 1, SC><<<stream_grid(L, n - done, 256), 256, 0, L.stream>>>(a, R, done, n,
+                                                                                                      d_in, out);
+}
+
 cudaError_t launch_reduce(const Launch &L, const ReduceArgs &a, int R, int fmt, int scaling, int d_out, int d_in,
                           float *out) {
   const size_t n = (size_t)d_out * d_in;
   bool vec = aligned16(out);
   for (int rr = 0; rr < R && vec; ++rr) vec = aligned16(a.codes[rr]);
   size_t done = 0;
-  const bool block = (scaling == GIFT_SCALE_BLOCK128);
   if (fmt == GIFT_FMT_F32) {
     if (vec) {
       k_reduce_f32_vec<<<stream_grid(L, n / 4, 256), 256, 0, L.stream>>>(a, R, n, out);
       done = (n / 4) * 4;
     }
-    if (done < n) k_reduce_scalar<3, false><<<stream_grid(L, n - done, 256), 256, 0, L.stream>>>(a, R, done, n, d_in, out);
+    if (done < n) k_reduce_scalar<3, 0><<<stream_grid(L, n - done, 256), 256, 0, L.stream>>>(a, R, done, n, d_in, out);
   } else if (fmt == GIFT_FMT_NVFP4) {
     bool v8 = aligned16(out);
     for (int rr = 0; rr < R && v8; ++rr) v8 = (((uintptr_t)a.codes[rr]) & 7u) == 0;
@@ -946,30 +1075,57 @@ cudaError_t launch_reduce(const Launch &L, const ReduceArgs &a, int R, int fmt, 
       k_reduce_nvfp4_vec<<<stream_grid(L, n / 16, 256), 256, 0, L.stream>>>(a, R, n, out);
       done = n;   // NVFP4 needs d_in % 16 == 0, so n % 16 == 0
     }
-    if (done < n) k_reduce_scalar<2, false><<<stream_grid(L, n - done, 256), 256, 0, L.stream>>>(a, R, done, n, d_in, out);
+    if (done < n) k_reduce_scalar<2, 0><<<stream_grid(L, n - done, 256), 256, 0, L.stream>>>(a, R, done, n, d_in, out);
   } else {
-    // block scales are looked up once per 16 elements: a group must not cross a row
-    if (vec && (!block || d_in % 16 == 0)) {
-      const int grid = stream_grid(L, n / 16, 256);
-      if (fmt == GIFT_FMT_E4M3) {
-        if (block) k_reduce_fp8_vec<FMT_E4M3, true><<<grid, 256, 0, L.stream>>>(a, R, n, d_in, out);
-        else k_reduce_fp8_vec<FMT_E4M3, false><<<grid, 256, 0, L.stream>>>(a, R, n, d_in, out);
-      } else {
-        if (block) k_reduce_fp8_vec<FMT_E5M2, true><<<grid, 256, 0, L.stream>>>(a, R, n, d_in, out);
-        else k_reduce_fp8_vec<FMT_E5M2, false><<<grid, 256, 0, L.stream>>>(a, R, n, d_in, out);
-      }
-      done = (n / 16) * 16;
+    // the vector path looks a scale up once per 16 elements: a group of 16 must not cross a
+    // 128-column tile edge (block 512 groups never cross a block)
+    const int sc = (scaling == GIFT_SCALE_BLOCK128) ? 1 : (scaling == GIFT_SCALE_BLOCK512) ? 2 : 0;
+    vec = vec && (sc != 1 || d_in % 16 == 0);
+    if (vec) done = (n / 16) * 16;
+    if (fmt == GIFT_FMT_E4M3) {
+      if (sc == 0) reduce_fp8<FMT_E4M3, 0>(L, a, R, n, done, d_in, out, vec);
+      else if (sc == 1) reduce_fp8<FMT_E4M3, 1>(L, a, R, n, done, d_in, out, vec);
+      else reduce_fp8<FMT_E4M3, 2>(L, a, R, n, done, d_in, out, vec);
+    } else {
+      if (sc == 0) reduce_fp8<FMT_E5M2, 0>(L, a, R, n, done, d_in, out, vec);
+      else if (sc == 1) reduce_fp8<FMT_E5M2, 1>(L, a, R, n, done, d_in, out, vec);
+      else reduce_fp8<FMT_E5M2, 2>(L, a, R, n, done, d_in, out, vec);
     }
-    if (done < n) {
-      const int grid = stream_grid(L, n - done, 256);
-      if (fmt == GIFT_FMT_E4M3) {
-        if (block) k_reduce_scalar<0, true><<<grid, 256, 0, L.stream>>>(a, R, done, n, d_in, out);
-        else k_reduce_scalar<0, false><<<grid, 256, 0, L.stream>>>(a, R, done, n, d_in, out);
-      } else {
-        if (block) k_reduce_scalar<1, true><<<grid, 256, 0, L.stream>>>(a, R, done, n, d_in, out);
-        else k_reduce_scalar<1, false><<<grid, 256, 0, L.stream>>>(a, R, done, n, d_in, out);
-      }
-    }
+  }
+  return cudaGetLastError();
+}
+
+template <int F, int MODE>
+static void block512_launch(const Launch &L, bool vec, const float *x, float *r, size_t n, const float *amax_in,
+                            uint8_t *codes, float *scales, float *amax_out, float *tout,
+                            unsigned long long *counts) {
+  const size_t nb = (n + kBlock1d - 1) / kBlock1d;
+  const int grid = stream_grid(L, nb, 8);   // 8 warps, one block each per step
+#define GIFT_B512(V, RS, TO) \
+  k_block512<F, MODE, V, RS, TO><<<grid, 256, 0, L.stream>>>(x, r, n, amax_in, codes, scales, amax_out, tout, counts, L.status)
+  if (vec) {
+    if (r) { if (tout) GIFT_B512(true, true, true); else GIFT_B512(true, true, false); }
+    else { if (tout) GIFT_B512(true, false, true); else GIFT_B512(true, false, false); }
+  } else {
+    if (r) { if (tout) GIFT_B512(false, true, true); else GIFT_B512(false, true, false); }
+    else { if (tout) GIFT_B512(false, false, true); else GIFT_B512(false, false, false); }
+  }
+#undef GIFT_B512
+}
+
+cudaError_t launch_block512(const Launch &L, int fmt, int mode, const float *x, float *r, size_t n,
+                            const float *amax_in, uint8_t *codes, float *scales, float *amax_out, float *tout,
+                            unsigned long long *counts) {
+  const bool vec = n % 4 == 0 && aligned16(x) && (!r || aligned16(r)) && (!tout || aligned16(tout)) &&
+                   (mode != 0 || (((uintptr_t)codes) & 3u) == 0);
+  if (fmt == GIFT_FMT_E4M3) {
+    if (mode == 0) block512_launch<FMT_E4M3, 0>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
+    else if (mode == 1) block512_launch<FMT_E4M3, 1>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
+    else block512_launch<FMT_E4M3, 2>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
+  } else {
+    if (mode == 0) block512_launch<FMT_E5M2, 0>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
+    else if (mode == 1) block512_launch<FMT_E5M2, 1>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
+    else block512_launch<FMT_E5M2, 2>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
   }
   return cudaGetLastError();
 }

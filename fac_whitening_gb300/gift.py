@@ -21,12 +21,13 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gift.h")
 # ---- enums (values fixed by include/gift.h) ---------------------------------------------
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NONFINITE, ERR_NOT_PD, ERR_TIMEOUT, ERR_NOT_CONVERGED = range(8)
 FMT = {"f32": 0, "e4m3": 1, "e5m2": 2, "nvfp4": 3}
-SCALING = {"tensor": 0, "block128": 1}
+SCALING = {"tensor": 0, "block128": 1, "block512": 2}
 XFORM = {"identity": 0, "lowrank": 1, "chol_input": 2, "chol_two_sided": 3}
 PREC = {"fp32": 0, "tc": 1}
 DTYPE = {"f32": 0, "bf16": 1}
 OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3, "kfac_factor": 4}
 OPT_SUBSPACE_ITERS = 0
+OPT_BARRIER_WAIT = 1
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int

@@ -78,8 +78,13 @@ typedef enum { GIFT_FMT_F32 = 0, GIFT_FMT_E4M3 = 1, GIFT_FMT_E5M2 = 2, GIFT_FMT_
  *  TENSOR   : one FP32 scale, scales[1].
  *  BLOCK128 : one FP32 scale per 128 x 128 tile, scales[ceil(d_out/128)][ceil(d_in/128)],
  *             edge tiles clipped.
+ *  BLOCK512 : one FP32 scale per 512 consecutive elements of the row-major tensor,
+ *             scales[ceil(d_out*d_in/512)], the last group shorter (the per-block Euclidean
+ *             baseline of the experiments, [notes] three simplifications: block size 512).
+ *             Identity and Cholesky transforms only (a rank-r factor returns
+ *             GIFT_ERR_UNSUPPORTED).
  * NVFP4 ignores this (its groups are fixed); F32 has no scales. */
-typedef enum { GIFT_SCALE_TENSOR = 0, GIFT_SCALE_BLOCK128 = 1 } gift_scaling;
+typedef enum { GIFT_SCALE_TENSOR = 0, GIFT_SCALE_BLOCK128 = 1, GIFT_SCALE_BLOCK512 = 2 } gift_scaling;
 
 /* Coordinate transforms ([notes] core idea eqs. (11), (14); simplification 1 eq. (16);
  * simplification 2 eq. (17)).
@@ -144,7 +149,12 @@ typedef enum {
 
 /* Tunables for gift_set_option. */
 typedef enum {
-  GIFT_OPT_SUBSPACE_ITERS = 0  /* power iterations of the rank-r sketch (default 10, 1..64) */
+  GIFT_OPT_SUBSPACE_ITERS = 0, /* power iterations of the rank-r sketch (default 10, 1..64)     */
+  GIFT_OPT_BARRIER_WAIT = 1    /* SM clock cycles a CTA of the shared-scale encode waits at its
+                                  grid-wide barrier before it gives up, writes GIFT_ERR_TIMEOUT
+                                  to d_status and stores no codes (default 2e9, about a second;
+                                  0..2e10).  A small value makes the wait run out on purpose: the
+                                  kernel still ends and the context stays usable. */
 } gift_option;
 
 /* Create a context for CUDA device `device` (queries its SM count).  Returns

@@ -55,7 +55,12 @@ def encode(f, W, fmt, scaling="tensor", amax_in=None, residual=None, Wt=None, pr
     kind = "identity" if f is None else f.kind
     codes, scales, tscale = alloc_codes(fmt, scaling, d_out, d_in)
     tout = torch.empty(d_out, d_in, dtype=torch.float32, device=DEV)
-    nam = 1 if (scaling == "tensor" or fmt == "nvfp4") else ((d_out + 127) // 128) * ((d_in + 127) // 128)
+    if scaling == "tensor" or fmt == "nvfp4":
+        nam = 1
+    elif scaling == "block512":
+        nam = (d_out * d_in + 511) // 512
+    else:
+        nam = ((d_out + 127) // 128) * ((d_in + 127) // 128)
     amax_out = torch.empty(nam, dtype=torch.float32, device=DEV)
     R = None if residual is None else t(residual)
     st = status()
@@ -74,7 +79,7 @@ def encode(f, W, fmt, scaling="tensor", amax_in=None, residual=None, Wt=None, pr
     else:
         out["codes"] = codes.cpu().numpy().reshape(d_out, d_in)
         sc = scales.cpu().numpy()
-        out["scales"] = sc if scaling == "tensor" else sc.reshape((d_out + 127) // 128, (d_in + 127) // 128)
+        out["scales"] = sc if scaling in ("tensor", "block512") else sc.reshape((d_out + 127) // 128, (d_in + 127) // 128)
     if R is not None:
         out["residual"] = R.cpu().numpy()
     out["_dev"] = (codes, scales, tscale)

@@ -96,7 +96,8 @@ def test_encode_nvfp4_unaligned():
 
 
 @pytest.mark.parametrize("fmt,scaling,shape", [("e4m3", "tensor", (64, 256)), ("e5m2", "block128", (200, 300)),
-                                               ("nvfp4", "tensor", (32, 64)), ("e4m3", "tensor", (17, 19))])
+                                               ("nvfp4", "tensor", (32, 64)), ("e4m3", "tensor", (17, 19)),
+                                               ("e4m3", "block512", (17, 19)), ("e5m2", "block512", (64, 256))])
 def test_error_feedback(fmt, scaling, shape):
     rng = np.random.default_rng(7)
     W = rng.standard_normal(shape).astype(np.float32)
@@ -121,12 +122,13 @@ def test_zero_tensor_and_nonfinite_status():
     assert encode(None, bad, "e5m2", "block128")["status"] == G.ERR_NONFINITE
 
 
-@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "block128"), ("nvfp4", "tensor")])
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "block128"), ("nvfp4", "tensor"),
+                                         ("e4m3", "block512")])
 def test_shared_amax_euclidean_path(fmt, scaling):
     # Algorithm 1, Euclidean path: Scale, AllReduceMax, Q with the shared scale
     rng = np.random.default_rng(8)
     Ws = [(rng.standard_normal((130, 256)) * (1 + r)).astype(np.float32) for r in range(4)]
-    nblk = 1 if scaling == "tensor" or fmt == "nvfp4" else 2 * 2
+    nblk = 1 if scaling == "tensor" or fmt == "nvfp4" else (2 * 2 if scaling == "block128" else 65)
     acc = torch.zeros(nblk, dtype=torch.float32, device=DEV)
     w = ws("amax", "identity", fmt, scaling, 130, 256)
     st = status()
@@ -136,6 +138,9 @@ def test_shared_amax_euclidean_path(fmt, scaling):
     if scaling == "tensor" or fmt == "nvfp4":
         shared = np.float32(max(O.abs_max(W) for W in Ws))
         assert acc.item() == shared
+    elif scaling == "block512":
+        shared = np.maximum.reduce([O.quantize(W, fmt, "block512")["amax"] for W in Ws])
+        np.testing.assert_array_equal(acc.cpu().numpy(), shared)
     else:
         shared = np.maximum.reduce([O.block_amax(W) for W in Ws])
         np.testing.assert_array_equal(acc.cpu().numpy().reshape(shared.shape), shared)
@@ -146,7 +151,9 @@ def test_shared_amax_euclidean_path(fmt, scaling):
 
 @pytest.mark.parametrize("fmt,scaling,R,shape", [("e4m3", "tensor", 8, (64, 256)), ("e5m2", "block128", 3, (200, 300)),
                                                  ("e4m3", "block128", 4, (256, 384)), ("nvfp4", "tensor", 4, (48, 64)),
-                                                 ("f32", "tensor", 4, (33, 35)), ("e4m3", "tensor", 5, (7, 9))])
+                                                 ("f32", "tensor", 4, (33, 35)), ("e4m3", "tensor", 5, (7, 9)),
+                                                 ("e4m3", "block512", 4, (33, 47)),
+                                                 ("e5m2", "block512", 3, (1536, 1536))])
 def test_replica_reduce(fmt, scaling, R, shape):
     rng = np.random.default_rng(9)
     Ws = [(rng.standard_normal(shape) * (0.5 + r)).astype(np.float32) for r in range(R)]
@@ -163,7 +170,8 @@ def test_replica_reduce(fmt, scaling, R, shape):
     np.testing.assert_array_equal(avg.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
 
-@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "block128"), ("nvfp4", "tensor")])
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("e5m2", "block128"), ("nvfp4", "tensor"),
+                                         ("e4m3", "block512")])
 def test_decode_identity_from_codes(fmt, scaling):
     rng = np.random.default_rng(10)
     W = rng.standard_normal((96, 160)).astype(np.float32)
@@ -177,7 +185,7 @@ def test_decode_identity_from_codes(fmt, scaling):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("scaling", ["tensor", "block128"])
+@pytest.mark.parametrize("scaling", ["tensor", "block128", "block512"])
 @pytest.mark.parametrize("shape", [(1536, 1536), (300, 200), (6144, 1536)])
 def test_boundary_hits(fmt, scaling, shape):
     from fac_whitening_gb300 import synth
@@ -190,3 +198,44 @@ def test_boundary_hits(fmt, scaling, shape):
     torch.cuda.synchronize()
     up, lo, n = O.boundary_hits(W, fmt, scaling)
     assert counts.cpu().tolist() == [2 * up, 2 * lo, 2 * n]
+
+
+@pytest.mark.parametrize("shape", [(1536, 6144), (37, 101), (64, 256)])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_encode_block512(shape, fmt):
+    # the per-block Euclidean baseline of the experiments: one scale per 512 consecutive
+    # elements, the last block shorter (37 x 101 = 3737 elements: ragged, not a multiple of 4)
+    from fac_whitening_gb300 import synth
+    W = synth.student_t_colscaled(*shape, seed=31 + shape[0]).numpy()
+    out = encode(None, W, fmt, "block512")
+    q = O.quantize(W, fmt, "block512")
+    assert out["status"] == 0
+    np.testing.assert_array_equal(out["codes"], q["codes"])
+    np.testing.assert_array_equal(out["scales"], q["scales"])
+    np.testing.assert_array_equal(out["amax"], q["amax"])
+    np.testing.assert_array_equal(out["tout"], W)
+
+
+def test_encode_block512_unaligned_and_transforms():
+    rng = np.random.default_rng(32)
+    base = torch.tensor(rng.standard_normal(64 * 33 + 1).astype(np.float32), device=DEV)
+    out = encode(None, None, "e5m2", "block512", Wt=base[1:].view(64, 33))   # 4-byte aligned only
+    np.testing.assert_array_equal(out["codes"], O.quantize(base[1:].view(64, 33).cpu().numpy(), "e5m2",
+                                                           "block512")["codes"])
+    # a Cholesky transform followed by the block-512 pack
+    from gpu_util import factor_to_gpu, rel_fro
+    A = np.cov(rng.standard_normal((96, 400))) + 0.1 * np.eye(96)
+    LA = O.cholesky(A).astype(np.float32)
+    LAi = O.lower_inverse(LA).astype(np.float32)
+    W = rng.standard_normal((40, 96)).astype(np.float32)
+    f = factor_to_gpu("chol_input", 40, 96, LA=LA, LAinv=LAi)
+    out = encode(f, W, "e4m3", "block512")
+    assert rel_fro(out["tout"], O.Xform("chol_input", LA=LA, LAinv=LAi).whiten(W)) <= 1e-5
+    np.testing.assert_array_equal(out["codes"], O.quantize(out["tout"], "e4m3", "block512")["codes"])
+    # a rank-r factor has no block-512 path
+    U = np.linalg.qr(rng.standard_normal((96, 8)))[0].astype(np.float32)
+    F = O.LowRankFactor(U, np.linspace(4, 1, 8).astype(np.float32), np.float32(0.1))
+    f = factor_to_gpu("lowrank", 40, 96, F=F)
+    with pytest.raises(G.GiftError) as e:
+        encode(f, W, "e4m3", "block512")
+    assert e.value.status == G.ERR_UNSUPPORTED
