@@ -97,17 +97,37 @@ struct FactorWs {
   double *A64 = nullptr, *Ai64 = nullptr, *work = nullptr;
   float *Gf = nullptr;
   double *G64 = nullptr, *Gi64 = nullptr;
-  void *at = nullptr;       // BF16 transpose of the activations (tensor-core SYRK)
+  void *at = nullptr;       // BF16 transpose of the activations (tensor-core SYRK), or the
+                            // activations' BF16 term planes (tensor-core FP32 SYRK)
+  size_t at_bytes = 0;
+  // LOWRANK on the tensor cores (FP32 refresh)
+  uint16_t *apl = nullptr, *qpl = nullptr;   // term planes of A (explicit sketch) and of Q^T
+  uint16_t *xpl = nullptr, *zpl = nullptr;   // term planes of FP32 activations (T rows) and of Z^T
+  float *Z = nullptr;                        // Z = a Q, T x 64
+  float *parts = nullptr;                    // split-K partials of A Q or a^T Z
+  int ksplit = 1;
+  bool implicit = true;
+  float *B32 = nullptr, *V32 = nullptr, *th = nullptr, *G32 = nullptr, *R32 = nullptr;
+  float *gparts = nullptr, *rparts = nullptr;
+  int *flag = nullptr;
   size_t bytes = 0;
 };
 
-FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in, int T) {
+// Bytes of the activations' BF16 term planes for the tensor-core K-FAC product: rows padded to
+// 128, T to 64; three planes cover FP32 activations, BF16 ones need one.
+size_t syrk_planes_bytes(int d, int T) {
+  const size_t rows = (size_t)(d + 127) / 128 * 128, ldk = (size_t)(T + 63) / 64 * 64;
+  return 3 * rows * ldk * 2;
+}
+
+FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in, int T, bool implicit = true) {
   FactorWs w;
   Carve c(base);
   w.A = c.take<float>((size_t)d_in * d_in);
   if (T > 0) {
     const int dmax = (kind == GIFT_XF_CHOL_TWO_SIDED && d_out > d_in) ? d_out : d_in;
-    w.at = c.take<uint8_t>(syrk_tc_scratch_bytes(dmax, T));
+    w.at_bytes = std::max(syrk_tc_scratch_bytes(dmax, T), syrk_planes_bytes(dmax, T));
+    w.at = c.take<uint8_t>(w.at_bytes);
   }
   if (kind == GIFT_XF_LOWRANK) {
     w.k = d_in < 64 ? d_in : 64;
@@ -131,6 +151,28 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
     w.ev = c.take<double>(64);
     w.tr = c.take<double>(1);
     w.sq = c.take<double>((size_t)trace_partials(sms));
+    if (w.k == 64 && d_in > 64 && T > 0) {
+      const size_t rows = (size_t)(d_in + 127) / 128 * 128, ldk = (size_t)(d_in + 63) / 64 * 64;
+      const size_t rows_t = (size_t)(T + 127) / 128 * 128, ldt = (size_t)(T + 63) / 64 * 64;
+      w.implicit = implicit;
+      if (!implicit) w.apl = c.take<uint16_t>(3 * rows * ldk);
+      w.qpl = c.take<uint16_t>(3 * 128 * ldk);
+      w.xpl = c.take<uint16_t>(3 * rows_t * ldk);   // FP32 activations only
+      w.zpl = c.take<uint16_t>(3 * 128 * ldt);
+      w.Z = c.take<float>((size_t)T * 64);
+      // split-K of the d-row products (A Q over K = d, or a^T Z over K = T)
+      const int tiles_m = (int)(rows / 128), nch = (int)((implicit ? ldt : ldk) / 64);
+      w.ksplit = std::max(1, std::min(sms / tiles_m, nch));
+      w.parts = c.take<float>(gemm_tc_parts_floats(d_in, 64, w.ksplit));
+      w.B32 = c.take<float>(64 * 64);
+      w.V32 = c.take<float>(64 * 64);
+      w.G32 = c.take<float>(64 * 64);
+      w.R32 = c.take<float>(64 * 64);
+      w.th = c.take<float>(64);
+      w.gparts = c.take<float>((size_t)refresh_gram_ctas(sms, std::max(d_in, T)) * 64 * 64);
+      w.rparts = c.take<float>((size_t)ritz_rotate_ctas(sms, d_in) * 64);
+      w.flag = c.take<int>(1);
+    }
   } else if (kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED) {
     const int nmax = d_in > d_out ? d_in : d_out;
     w.A64 = c.take<double>((size_t)d_in * d_in);
@@ -273,8 +315,9 @@ gift_status gift_create(gift_ctx **ctx, int device) {
   if (!c) return GIFT_ERR_CUDA;
   c->device = device;
   c->sms = sms;
-  c->subspace_iters = 10;
+  c->subspace_iters = 16;
   c->barrier_wait = kDefaultBarrierWait;
+  c->sketch = 0;
   *ctx = c;
   return GIFT_OK;
 }
@@ -286,6 +329,11 @@ gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value) {
   if (opt == GIFT_OPT_SUBSPACE_ITERS) {
     if (value < 1 || value > 64) return GIFT_ERR_INVALID_ARG;
     ctx->subspace_iters = (int)value;
+    return GIFT_OK;
+  }
+  if (opt == GIFT_OPT_SKETCH) {
+    if (value != 0 && value != 1) return GIFT_ERR_INVALID_ARG;
+    ctx->sketch = (int)value;
     return GIFT_OK;
   }
   if (opt == GIFT_OPT_BARRIER_WAIT) {
@@ -317,10 +365,11 @@ size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gi
   (void)rank;
   if (!ctx || d_out <= 0 || d_in <= 0 || !valid_kind(kind) || !valid_fmt(fmt) || !valid_scaling(scaling))
     return (size_t)-1;
-  if (op == GIFT_OP_KFAC_FACTOR) return T > 0 ? syrk_tc_scratch_bytes(d_in, T) : (size_t)-1;
+  if (op == GIFT_OP_KFAC_FACTOR)
+    return T > 0 ? std::max(syrk_tc_scratch_bytes(d_in, T), syrk_planes_bytes(d_in, T)) : (size_t)-1;
   if (op == GIFT_OP_FACTOR_UPDATE) {
     if (kind == GIFT_XF_IDENTITY) return 0;
-    return factor_layout(nullptr, ctx->sms, kind, d_out, d_in, T).bytes;
+    return factor_layout(nullptr, ctx->sms, kind, d_out, d_in, T, ctx->sketch == 0).bytes;
   }
   if (op != GIFT_OP_ENCODE && op != GIFT_OP_DECODE && op != GIFT_OP_AMAX) return (size_t)-1;
   return codec_layout(nullptr, ctx->sms, op, kind, d_out, d_in).bytes;
@@ -353,13 +402,49 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
 // -----------------------------------------------------------------------------------------
 namespace {
 
-// A = x^T x / T (full symmetric, FP32): tensor cores for TC precision and BF16 input where the
-// shape allows (at = scratch of syrk_tc_scratch_bytes(d, T) bytes), FP32 SIMT otherwise.
-cudaError_t kfac_syrk(const Launch &L, const void *x, bool bf16, int T, int d, gift_precision prec, void *at,
-                      float *out) {
-  if (prec == GIFT_PREC_TC && bf16 && at && syrk_tc_ok(d, T, x, at, out)) {
-    cudaError_t e = launch_syrk_tc(L, x, T, d, 1.0f / (float)T, at, out);
+// A = x^T x / T (full symmetric, FP32).
+//  TC precision, BF16 x: k_syrk_tc (exact products, the tensor core's accumulation over T).
+//  FP32 precision with a workspace of syrk_planes_bytes: the tensor-core GEMM on the exact BF16
+//    terms of x (one term for BF16 x, three for FP32 x and the six products i + j <= 2), a fresh
+//    accumulator per 64 tokens summed round to nearest: FP32 accuracy.
+//  Otherwise FP32 SIMT.
+cudaError_t kfac_syrk(const Launch &L, const void *x, bool bf16, int T, int d, gift_precision prec, void *ws,
+                      size_t ws_bytes, float *out) {
+  if (prec == GIFT_PREC_TC && bf16 && ws && ws_bytes >= syrk_tc_scratch_bytes(d, T) &&
+      syrk_tc_ok(d, T, x, ws, out)) {
+    cudaError_t e = launch_syrk_tc(L, x, T, d, 1.0f / (float)T, ws, out);
     if (e != cudaSuccess) return e;
+    return launch_mirror_lower(L, out, d);
+  }
+  const bool tc_planes = ws && ws_bytes >= syrk_planes_bytes(d, T) && aligned16(ws) && aligned16(out) &&
+                         (!bf16 || (d % 64 == 0 && T % 64 == 0 && aligned16(x)));
+  if (tc_planes) {
+    uint16_t *pl = static_cast<uint16_t *>(ws);
+    const int rows = (d + 127) / 128 * 128, ldk = (T + 63) / 64 * 64;
+    cudaError_t e;
+    int nt = 3;
+    if (bf16) {   // the transpose is the single term plane (T % 64 == 0: ldk = T)
+      nt = 1;
+      if ((e = launch_transpose_bf16(L, x, T, d, pl)) != cudaSuccess) return e;
+      if (rows > d && (e = cudaMemsetAsync(pl + (size_t)d * ldk, 0, (size_t)(rows - d) * ldk * 2, L.stream)) !=
+                          cudaSuccess)
+        return e;
+    } else if ((e = launch_split_planes(L, static_cast<const float *>(x), d, T, d, true, 3, pl)) != cudaSuccess) {
+      return e;
+    }
+    GemmPlanes g;
+    g.pa = pl;
+    g.pb = pl;
+    g.M = d;
+    g.N = d;
+    g.K = T;
+    g.nta = g.ntb = nt;
+    g.fp32 = true;
+    g.lower_tiles = true;
+    g.alpha = 1.0f / (float)T;
+    g.C = out;
+    g.ldc = d;
+    if ((e = launch_gemm_planes(L, g)) != cudaSuccess) return e;
     return launch_mirror_lower(L, out, d);
   }
   GemmArgs g{};
@@ -392,7 +477,7 @@ gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int 
   if (prec != GIFT_PREC_FP32 && prec != GIFT_PREC_TC) return GIFT_ERR_INVALID_ARG;
   if (prec == GIFT_PREC_TC && (!ws || ws_bytes < syrk_tc_scratch_bytes(d, T))) return GIFT_ERR_INVALID_ARG;
   const Launch L = mk(ctx, d_status, stream);
-  CK(kfac_syrk(L, a, a_dt == GIFT_DT_BF16, T, d, prec, prec == GIFT_PREC_TC ? ws : nullptr, A_out));
+  CK(kfac_syrk(L, a, a_dt == GIFT_DT_BF16, T, d, prec, ws, ws ? ws_bytes : 0, A_out));
   return GIFT_OK;
 }
 
@@ -409,16 +494,123 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
   if (cs != GIFT_OK) return cs;
   if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!delta || (d_dt != GIFT_DT_F32 && d_dt != GIFT_DT_BF16)))
     return GIFT_ERR_INVALID_ARG;
-  const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in, T);
+  const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in, T, ctx->sketch == 0);
   if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
-  const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in, T);
+  const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in, T, ctx->sketch == 0);
   const Launch L = mk(ctx, d_status, stream);
 
   // A = a^T a / T (lower tiles, then mirrored)
   auto syrk = [&](const void *x, bool bf16, int d, float *out) -> cudaError_t {
-    return kfac_syrk(L, x, bf16, T, d, prec, w.at, out);
+    return kfac_syrk(L, x, bf16, T, d, prec, w.at, w.at_bytes, out);
   };
-  CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
+  if (!(f->kind == GIFT_XF_LOWRANK && w.qpl)) CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
+
+  if (f->kind == GIFT_XF_LOWRANK && w.qpl) {
+    // FP32 subspace iteration with Rayleigh-Ritz steps, the products on the tensor cores
+    const int k = 64, r = f->rank;
+    const bool bf16 = (a_dt == GIFT_DT_BF16);
+    const int nt = (prec == GIFT_PREC_TC) ? 2 : 3;   // terms of the FP32 operands
+    const bool fp32 = (prec != GIFT_PREC_TC);
+    const int *skip = w.flag;
+    // the activations as the A operand of Z = a Q (M = T, K = d_in): BF16 rows as they are,
+    // FP32 ones split into terms
+    const bool a_plain = bf16 && d_in % 8 == 0 && aligned16(a);
+    if (!a_plain) {
+      if (bf16) CK(launch_split_planes_bf16(L, a, T, d_in, d_in, false, w.xpl));
+      else CK(launch_split_planes(L, static_cast<const float *>(a), T, d_in, d_in, false, nt, w.xpl));
+    }
+    const int a_nt = bf16 ? 1 : nt;
+    if (w.implicit) {
+      // a^T as the A operand of Y = a^T Z / T (M = d_in, K = T), in the K-FAC workspace
+      if (bf16) CK(launch_split_planes_bf16(L, a, d_in, T, d_in, true, static_cast<uint16_t *>(w.at)));
+      else CK(launch_split_planes(L, static_cast<const float *>(a), d_in, T, d_in, true, nt,
+                                  static_cast<uint16_t *>(w.at)));
+      if (aligned16(a)) CK(launch_trace_acts32(L, a, bf16, T, d_in, w.sq, trace_partials(ctx->sms), w.tr));
+      else CK(launch_trace_from_activations(L, a, bf16, T, d_in, w.sq, w.tr));
+    } else {
+      CK(syrk(a, bf16, d_in, w.A));
+      CK(launch_trace_diag(L, w.A, d_in, w.tr));
+      CK(launch_split_planes(L, w.A, d_in, d_in, d_in, false, nt, w.apl));
+    }
+    CK(cudaMemsetAsync(w.flag, 0, sizeof(int), stream));
+    auto orth = [&](float *Y, const int *sk) -> cudaError_t {   // Q = Y R^-1, twice (CholQR2)
+      cudaError_t e = cudaSuccess;
+      const float *src = Y;
+      for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+        if ((e = launch_gram_tall(L, src, src, d_in, k, w.gparts, w.G32, true, sk)) != cudaSuccess) break;
+        if ((e = launch_chol_rinv32(L, w.G32, k, w.R32, sk)) != cudaSuccess) break;
+        e = launch_right_mul64(L, src, d_in, w.R32, w.Q, sk);
+        src = w.Q;
+      }
+      return e;
+    };
+    auto gemm = [&](const uint16_t *pa, int a_ld, int nta, const uint16_t *pb, int M, int K, float alpha, float *C,
+                    int ksplit, const int *sk) -> cudaError_t {
+      GemmPlanes g;
+      g.pa = pa;
+      g.a_ld = a_ld;
+      g.pb = pb;
+      g.M = M;
+      g.N = k;
+      g.K = K;
+      g.nta = nta;
+      g.ntb = nt;
+      g.fp32 = fp32;
+      g.ksplit = ksplit;
+      g.parts = w.parts;
+      g.alpha = alpha;
+      g.C = C;
+      g.ldc = k;
+      g.skip = sk;
+      return launch_gemm_planes(L, g);
+    };
+    auto za = [&](const int *sk) -> cudaError_t {   // Z = a Q
+      cudaError_t e = launch_split_planes(L, w.Q, k, d_in, k, true, nt, w.qpl, sk);
+      if (e != cudaSuccess) return e;
+      return gemm(a_plain ? static_cast<const uint16_t *>(a) : w.xpl, a_plain ? d_in : 0, a_nt, w.qpl, T, d_in, 1.0f,
+                  w.Z, 1, sk);
+    };
+    auto sketch = [&](const int *sk) -> cudaError_t {   // Y = A Q
+      cudaError_t e;
+      if (w.implicit) {   // A Q = a^T (a Q) / T
+        if ((e = za(sk)) != cudaSuccess) return e;
+        if ((e = launch_split_planes(L, w.Z, k, T, k, true, nt, w.zpl, sk)) != cudaSuccess) return e;
+        e = gemm(static_cast<const uint16_t *>(w.at), 0, a_nt, w.zpl, d_in, T, 1.0f / (float)T, w.Y, w.ksplit, sk);
+      } else {
+        if ((e = launch_split_planes(L, w.Q, k, d_in, k, true, nt, w.qpl, sk)) != cudaSuccess) return e;
+        e = gemm(w.apl, 0, nt, w.qpl, d_in, d_in, 1.0f, w.Y, w.ksplit, sk);
+      }
+      return e;
+    };
+    auto ritz = [&](const int *sk) -> cudaError_t {   // B = Q^T Y; (theta, V) = eig(B); Y <- Y V
+      cudaError_t e = launch_gram_tall(L, w.Q, w.Y, d_in, k, w.gparts, w.B32, true, sk);
+      if (e != cudaSuccess) return e;
+      // the Ritz directions condition the next CholQR: a few sweeps are enough
+      if ((e = launch_jacobi32(L, w.B32, k, w.th, w.V32, 2, false, sk)) != cudaSuccess) return e;
+      if ((e = launch_ritz_rotate(L, w.Y, w.Q, d_in, w.V32, w.th, w.rparts, sk)) != cudaSuccess) return e;
+      return launch_ritz_check(L, w.rparts, ritz_rotate_ctas(ctx->sms, d_in), w.th, r, w.flag);
+    };
+    CK(launch_philox_gaussian(L, w.Y, (size_t)d_in * k, seed));
+    CK(orth(w.Y, nullptr));
+    for (int it = 0; it < ctx->subspace_iters; ++it) {
+      CK(sketch(skip));
+      // Rayleigh-Ritz on the first two iterations (the random start gives a badly conditioned
+      // A Q), then every fourth with the convergence test; in between the basis stays close to
+      // the Ritz directions, so A Q keeps nearly orthogonal columns
+      if (it < 2 || it % 4 == 3) CK(ritz(skip));
+      CK(orth(w.Y, skip));
+    }
+    // final Rayleigh-Ritz step from the activations: B = Q^T A Q = (a Q)^T (a Q) / T, a Gram
+    // matrix (no cancellation between large and small eigenvalues), solved to convergence
+    CK(za(nullptr));
+    CK(launch_gram_tall(L, w.Z, w.Z, T, k, w.gparts, w.B32, true, nullptr, 1.0f / (float)T));
+    CK(launch_jacobi32(L, w.B32, k, w.th, w.V32, 40, true, nullptr));
+    CK(launch_f32_to_f64(L, w.V32, w.V, (size_t)k * k));
+    CK(launch_f32_to_f64(L, w.th, w.ev, (size_t)k));
+    CK(launch_lowrank_outputs(L, w.Q, d_in, k, w.V, w.ev, w.tr, r, f->U, f->mu, f->sigma));
+    if (f->planes) CK(launch_lr_factor_planes(L, f->U, d_in, r, f->planes));
+    return GIFT_OK;
+  }
 
   if (f->kind == GIFT_XF_LOWRANK) {
     const int k = w.k;

@@ -9,6 +9,7 @@ struct gift_ctx {
   int sms;
   int subspace_iters;
   long long barrier_wait;   // clock cycles a CTA waits at a streaming grid barrier
+  int sketch;               // rank-r refresh: 0 implicit a^T (a Q) / T, 1 explicit A Q
 };
 
 namespace gift {
@@ -171,6 +172,32 @@ cudaError_t launch_lr_proj_tc(const Launch &L, const float *X, int d_out, int d_
 bool syrk_tc_ok(int d, int T, const void *a, const void *at, const float *out);
 size_t syrk_tc_scratch_bytes(int d, int T);
 cudaError_t launch_syrk_tc(const Launch &L, const void *a, int T, int d, float scale, void *at, float *out);
+// a (T x d BF16, d and T multiples of 64) -> at (d x T)
+cudaError_t launch_transpose_bf16(const Launch &L, const void *a, int T, int d, void *at);
+
+// factor_tc.cu: the FP32 pieces of the rank-r refresh (k = 64 sketch columns); every launch
+// returns at once while *skip != 0 (skip nullable)
+int refresh_gram_ctas(int sms, int d);
+// out (k x k) = X^T Y for d x k X and Y; parts holds refresh_gram_ctas x k x k floats
+cudaError_t launch_gram_tall(const Launch &L, const float *X, const float *Y, int d, int k, float *parts, float *out,
+                             bool sym, const int *skip, float scale = 1.0f);
+// tr(a^T a / T) from the activations; part holds nparts doubles (one per CTA)
+cudaError_t launch_trace_acts32(const Launch &L, const void *a, bool bf16, int T, int d, double *part, int nparts,
+                                double *tr);
+cudaError_t launch_chol_rinv32(const Launch &L, const float *G, int k, float *Rinv, const int *skip);
+// at most max_sweeps sweeps; report: NOT_CONVERGED into the status word when they run out
+cudaError_t launch_jacobi32(const Launch &L, const float *B, int k, float *evals, float *V, int max_sweeps,
+                            bool report, const int *skip);
+// out = X M for X d x 64 and M 64 x 64 (out may be X)
+cudaError_t launch_right_mul64(const Launch &L, const float *X, int d, const float *M, float *out, const int *skip);
+// Y <- Y V in place with the Ritz residuals' partial sums of squares (ritz_rotate_ctas x 64
+// floats), then the convergence flag from them
+int ritz_rotate_ctas(int sms, int d);
+cudaError_t launch_ritz_rotate(const Launch &L, float *Y, const float *Q, int d, const float *V, const float *theta,
+                               float *res_parts, const int *skip);
+cudaError_t launch_ritz_check(const Launch &L, const float *res_parts, int nparts, const float *theta, int r,
+                              int *flag);
+cudaError_t launch_trace_diag(const Launch &L, const float *A, int d, double *tr);
 
 // Sets a kernel's opt-in dynamic shared-memory size once per device and kernel (so no
 // attribute call happens inside a stream capture after the first eager call).  Keyed on the
@@ -212,12 +239,37 @@ bool gemm_tc_ok(const GemmArgs &g, const void *ws);
 size_t gemm_tc_ws_bytes(int M, int N, int K, int nterms);
 size_t gemm_tc_plane_bytes(int rows, int K, int nterms);
 cudaError_t launch_gemm_tc(const Launch &L, const GemmArgs &g, int nt, void *ws);
-// The planes alone (rows x K, or the transpose of a K x rows source), and the product of two
-// plane sets C = alpha A B^T; a_lower / b_lower: row i of A (row j of B) is zero beyond k = i (j).
+// The planes alone (rows x K, or the transpose of a K x rows source; rows padded to 128 and K
+// to 64 with zeros), and the product of two plane sets C = alpha A B^T (M x N, K):
+//   nta / ntb   term planes of A and B (1..3; a BF16 source is its own single term);
+//   fp32        keep the products x_i y_j with i + j <= 2 (0-based), else i + j <= 1;
+//   a_lower / b_lower  row i of A (row j of B) is zero beyond k = i (j);
+//   lower_tiles only the 128 x 128 tiles on or below the diagonal (M == N; mirror after);
+//   ksplit > 1  K in ksplit slices, partial products in parts (gemm_tc_parts_floats floats),
+//               then summed in slice order;
+//   skip        nullable device flag: every launch does nothing while it is non-zero.
+struct GemmPlanes {
+  const uint16_t *pa = nullptr, *pb = nullptr;
+  int a_ld = 0, b_ld = 0;   // > 0: the operand is a plain BF16 matrix (one term, M or N rows of
+                            // this many elements, a multiple of 8) instead of padded planes
+  int M = 0, N = 0, K = 0;
+  int nta = 1, ntb = 1;
+  bool fp32 = true;
+  bool a_lower = false, b_lower = false, lower_tiles = false;
+  int ksplit = 1;
+  float *parts = nullptr;
+  float alpha = 1.0f;
+  float *C = nullptr;
+  int ldc = 0;
+  const int *skip = nullptr;
+};
 cudaError_t launch_split_planes(const Launch &L, const float *src, int rows, int K, int ld, bool transpose, int nt,
-                                uint16_t *planes);
-cudaError_t launch_gemm_planes(const Launch &L, const uint16_t *pa, const uint16_t *pb, int M, int N, int K, int nt,
-                               bool a_lower, bool b_lower, float alpha, float *C, int ldc);
+                                uint16_t *planes, const int *skip = nullptr);
+cudaError_t launch_gemm_planes(const Launch &L, const GemmPlanes &g);
+// the single-term planes of a BF16 source
+cudaError_t launch_split_planes_bf16(const Launch &L, const void *src, int rows, int K, int ld, bool transpose,
+                                     uint16_t *planes, const int *skip = nullptr);
+size_t gemm_tc_parts_floats(int M, int N, int ksplit);
 cudaError_t launch_sgemm_splitk(const Launch &L, const GemmArgs &g, float *parts, int splits);
 size_t sgemm_splitk_parts(int M, int ldc, int splits);
 // C = alpha * op(A) op(B) + beta * C in FP64 with float or double operands, split-K slices

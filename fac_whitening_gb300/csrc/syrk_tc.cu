@@ -272,6 +272,12 @@ bool syrk_tc_ok(int d, int T, const void *a, const void *at, const float *out) {
 
 size_t syrk_tc_scratch_bytes(int d, int T) { return (size_t)d * T * 2; }
 
+cudaError_t launch_transpose_bf16(const Launch &L, const void *a, int T, int d, void *at) {
+  k_transpose_bf16<<<dim3(d / 64, T / 64), 256, 0, L.stream>>>(static_cast<const uint16_t *>(a), T, d,
+                                                                static_cast<uint16_t *>(at));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_syrk_tc(const Launch &L, const void *a, int T, int d, float scale, void *at, float *out) {
   k_transpose_bf16<<<dim3(d / 64, T / 64), 256, 0, L.stream>>>(static_cast<const uint16_t *>(a), T, d,
                                                                 static_cast<uint16_t *>(at));

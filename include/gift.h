@@ -149,7 +149,12 @@ typedef enum {
 
 /* Tunables for gift_set_option. */
 typedef enum {
-  GIFT_OPT_SUBSPACE_ITERS = 0, /* power iterations of the rank-r sketch (default 10, 1..64)     */
+  GIFT_OPT_SUBSPACE_ITERS = 0, /* most power iterations of the rank-r sketch (default 16, 1..64);
+                                  they stop earlier once the top Ritz pairs have converged */
+  GIFT_OPT_SKETCH = 2,         /* rank-r refresh: 0 (default) forms A Q as a^T (a Q) / T from the
+                                  activations and never forms A; 1 forms A = a^T a / T (the
+                                  K-FAC product) and multiplies it.  Set it before
+                                  gift_workspace_bytes: the two need different workspaces. */
   GIFT_OPT_BARRIER_WAIT = 1    /* SM clock cycles a CTA of the shared-scale encode waits at its
                                   grid-wide barrier before it gives up, writes GIFT_ERR_TIMEOUT
                                   to d_status and stores no codes (default 2e9, about a second;

@@ -14,9 +14,10 @@ from gpu_util import DEV, ctx, rel_fro, status, t
 pytestmark = pytest.mark.gpu
 
 
-def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None, prec="fp32"):
+def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None, prec="fp32", sketch=0):
     d_in = a.shape[1]
     f = G.Factor.empty(kind, d_out, d_in, rank)
+    G.gift_set_option(ctx(), G.OPT_SKETCH, sketch)
     n = G.gift_workspace_bytes(ctx(), "factor_update", kind, "e4m3", "tensor", d_out, d_in, a.shape[0], rank)
     w = torch.zeros(n, dtype=torch.uint8, device=DEV)
     st = status()
@@ -25,7 +26,8 @@ def run_factor(kind, a, d_out, rank=32, delta=None, seed=7, iters=None, prec="fp
     G.gift_factor_update(ctx(), f, a, delta=delta, seed=seed, prec=prec, ws=w, status=st)
     torch.cuda.synchronize()
     if iters:
-        G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, 10)
+        G.gift_set_option(ctx(), G.OPT_SUBSPACE_ITERS, 16)
+    G.gift_set_option(ctx(), G.OPT_SKETCH, 0)
     return f, w, int(st.item())
 
 
@@ -52,17 +54,22 @@ def check_lowrank(f, a64, rank, st, sigma_rtol=1e-3):
 def test_factor_lowrank_tiny():
     spec = synth.tiny_workload().layers[0]
     _, a = synth.layer_inputs(spec, 0, 0, 1)
-    f, w, st = run_factor("lowrank", t(a), 64)
+    f, w, st = run_factor("lowrank", t(a), 64, sketch=1)   # explicit: A is formed
+    check_lowrank(f, a.double().numpy(), 32, st)
+    f, _, st = run_factor("lowrank", t(a), 64)              # implicit
     check_lowrank(f, a.double().numpy(), 32, st)
     # the SYRK result sits at the start of the workspace: A = a^T a / T
     A_gpu = w[: 256 * 256 * 4].view(torch.float32).view(256, 256).cpu().double().numpy()
     assert rel_fro(A_gpu, O.kfac_factor(a.double().numpy())) <= 1e-6
 
 
-def test_factor_lowrank_bf16_steep():
+@pytest.mark.parametrize("sketch", [0, 1], ids=["implicit", "explicit"])
+def test_factor_lowrank_bf16_steep(sketch):
+    # the steepest spectrum of the 600M-like layers (exponent 1.2: mu_32 / mu_1 = 2.5e-4); the
+    # sketch A Q formed from the activations (a^T (a Q) / T, A never formed) or from A
     spec = synth.LayerSpec("m", 128, 1024, T=4096, exponent=1.2, act_dtype=torch.bfloat16)
     _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
-    f, _, st = run_factor("lowrank", a, 128)
+    f, _, st = run_factor("lowrank", a, 128, sketch=sketch)
     check_lowrank(f, a.double().cpu().numpy(), 32, st)
 
 
@@ -74,7 +81,7 @@ def test_factor_tc_syrk_exact_on_integer_activations():
     T, d = 1024, 512
     a = rng.integers(-2, 3, size=(T, d)).astype(np.float32)
     at = torch.tensor(a, dtype=torch.bfloat16, device=DEV)
-    f, w, st = run_factor("lowrank", at, 256, prec="tc")
+    f, w, st = run_factor("lowrank", at, 256, prec="tc", sketch=1)
     assert st == 0
     A_gpu = w[: d * d * 4].view(torch.float32).view(d, d).cpu().double().numpy()
     np.testing.assert_array_equal(A_gpu, (a.astype(np.float64).T @ a.astype(np.float64)) / T)
@@ -88,7 +95,7 @@ def test_factor_lowrank_bf16_steep_tc():
     # sigma^-1/2 moves by half of sigma's relative error, 1e-2 -> 5e-3 < 2e-2
     spec = synth.LayerSpec("m", 128, 1024, T=4096, exponent=1.2, act_dtype=torch.bfloat16)
     _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
-    f, w, st = run_factor("lowrank", a, 128, prec="tc")
+    f, w, st = run_factor("lowrank", a, 128, prec="tc", sketch=1)
     a64 = a.double().cpu().numpy()
     check_lowrank(f, a64, 32, st, sigma_rtol=1e-2)
     A_gpu = w[: 1024 * 1024 * 4].view(torch.float32).view(1024, 1024).cpu().double().numpy()
@@ -157,3 +164,34 @@ def test_philox_start_is_seeded():
     f3, _, _ = run_factor("lowrank", t(a), 64, seed=2)
     assert torch.equal(f1.U, f2.U) and torch.equal(f1.mu, f2.mu)
     np.testing.assert_allclose(f1.mu.cpu().numpy(), f3.mu.cpu().numpy(), rtol=1e-4)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_factor_fp32_tc_syrk_exact_on_integer_activations(dtype):
+    # the FP32-precision K-FAC product on the tensor cores (exact BF16 terms, one accumulator per
+    # 64 tokens, round-to-nearest sums): with small integer activations every partial sum is an
+    # exact FP32 integer, so A = a^T a / T exactly, ragged row tiles and the mirror included
+    rng = np.random.default_rng(12)
+    T, d = 1024, 320
+    a = rng.integers(-3, 4, size=(T, d)).astype(np.float32)
+    at = torch.tensor(a, dtype=dtype, device=DEV)
+    A = torch.empty(d, d, device=DEV)
+    n = G.gift_workspace_bytes(ctx(), "kfac_factor", "identity", "e4m3", "tensor", d, d, T)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    st = status()
+    G.gift_kfac_factor(ctx(), at, A, prec="fp32", ws=w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(A.cpu().double().numpy(), (a.astype(np.float64).T @ a.astype(np.float64)) / T)
+
+
+def test_refresh_iterations_stop_when_ritz_values_settle():
+    # the convergence stop: a cap of 40 iterations gives the same factor as a cap of 12 once the
+    # Ritz values have settled (the remaining iterations do nothing)
+    spec = synth.LayerSpec("m", 128, 1024, T=4096, exponent=0.8, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 9, 4, 1, device="cuda")
+    f12, _, st12 = run_factor("lowrank", a, 128, iters=12)
+    f40, _, st40 = run_factor("lowrank", a, 128, iters=40)
+    assert st12 == 0 and st40 == 0
+    assert torch.equal(f12.mu, f40.mu) and torch.equal(f12.U, f40.U)
+    check_lowrank(f40, a.double().cpu().numpy(), 32, st40)

@@ -56,7 +56,9 @@ def test_c2_cholesky_factors_full_size(c2):
         # same FP32 K-FAC product gift_kfac_factor returns): FP64 on both sides, so the only
         # difference is L and L^-1 rounded to FP32.
         Ag = torch.empty(d, d, device=DEV)
-        G.gift_kfac_factor(ctx(), x.to(DEV), Ag, prec="fp32", status=status())
+        n = G.gift_workspace_bytes(ctx(), "kfac_factor", "identity", "e4m3", "tensor", d, d, x.shape[0])
+        G.gift_kfac_factor(ctx(), x.to(DEV), Ag, prec="fp32", ws=torch.zeros(n, dtype=torch.uint8, device=DEV),
+                           status=status())
         torch.cuda.synchronize()
         Lo = O.cholesky(Ag.cpu().double().numpy())
         assert rel_fro(L, Lo) <= 1e-6
