@@ -157,7 +157,7 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
       w.implicit = implicit;
       if (!implicit) w.apl = c.take<uint16_t>(3 * rows * ldk);
       w.qpl = c.take<uint16_t>(3 * 128 * ldk);
-      w.xpl = c.take<uint16_t>(3 * rows_t * ldk);   // FP32 activations only
+      w.xpl = c.take<uint16_t>(3 * rows_t * ldk);   // the activations as term planes
       w.zpl = c.take<uint16_t>(3 * 128 * ldt);
       w.Z = c.take<float>((size_t)T * 64);
       // split-K of the d-row products (A Q over K = d, or a^T Z over K = T)
@@ -416,19 +416,17 @@ cudaError_t kfac_syrk(const Launch &L, const void *x, bool bf16, int T, int d, g
     if (e != cudaSuccess) return e;
     return launch_mirror_lower(L, out, d);
   }
-  const bool tc_planes = ws && ws_bytes >= syrk_planes_bytes(d, T) && aligned16(ws) && aligned16(out) &&
-                         (!bf16 || (d % 64 == 0 && T % 64 == 0 && aligned16(x)));
+  const bool tc_planes = ws && ws_bytes >= syrk_planes_bytes(d, T) && aligned16(ws) && aligned16(out);
   if (tc_planes) {
     uint16_t *pl = static_cast<uint16_t *>(ws);
     const int rows = (d + 127) / 128 * 128, ldk = (T + 63) / 64 * 64;
     cudaError_t e;
     int nt = 3;
-    if (bf16) {   // the transpose is the single term plane (T % 64 == 0: ldk = T)
+    (void)rows;
+    (void)ldk;
+    if (bf16) {   // a BF16 value is its own single term
       nt = 1;
-      if ((e = launch_transpose_bf16(L, x, T, d, pl)) != cudaSuccess) return e;
-      if (rows > d && (e = cudaMemsetAsync(pl + (size_t)d * ldk, 0, (size_t)(rows - d) * ldk * 2, L.stream)) !=
-                          cudaSuccess)
-        return e;
+      if ((e = launch_split_planes_bf16(L, x, d, T, d, true, pl)) != cudaSuccess) return e;
     } else if ((e = launch_split_planes(L, static_cast<const float *>(x), d, T, d, true, 3, pl)) != cudaSuccess) {
       return e;
     }
@@ -512,13 +510,10 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
     const int nt = (prec == GIFT_PREC_TC) ? 2 : 3;   // terms of the FP32 operands
     const bool fp32 = (prec != GIFT_PREC_TC);
     const int *skip = w.flag;
-    // the activations as the A operand of Z = a Q (M = T, K = d_in): BF16 rows as they are,
-    // FP32 ones split into terms
-    const bool a_plain = bf16 && d_in % 8 == 0 && aligned16(a);
-    if (!a_plain) {
-      if (bf16) CK(launch_split_planes_bf16(L, a, T, d_in, d_in, false, w.xpl));
-      else CK(launch_split_planes(L, static_cast<const float *>(a), T, d_in, d_in, false, nt, w.xpl));
-    }
+    // the activations as the A operand of Z = a Q (M = T, K = d_in): one term for BF16, split
+    // into terms for FP32
+    if (bf16) CK(launch_split_planes_bf16(L, a, T, d_in, d_in, false, w.xpl));
+    else CK(launch_split_planes(L, static_cast<const float *>(a), T, d_in, d_in, false, nt, w.xpl));
     const int a_nt = bf16 ? 1 : nt;
     if (w.implicit) {
       // a^T as the A operand of Y = a^T Z / T (M = d_in, K = T), in the K-FAC workspace
@@ -544,11 +539,10 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
       }
       return e;
     };
-    auto gemm = [&](const uint16_t *pa, int a_ld, int nta, const uint16_t *pb, int M, int K, float alpha, float *C,
-                    int ksplit, const int *sk) -> cudaError_t {
+    auto gemm = [&](const uint16_t *pa, int nta, const uint16_t *pb, int M, int K, float alpha, float *C, int ksplit,
+                    const int *sk) -> cudaError_t {
       GemmPlanes g;
       g.pa = pa;
-      g.a_ld = a_ld;
       g.pb = pb;
       g.M = M;
       g.N = k;
@@ -567,18 +561,17 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
     auto za = [&](const int *sk) -> cudaError_t {   // Z = a Q
       cudaError_t e = launch_split_planes(L, w.Q, k, d_in, k, true, nt, w.qpl, sk);
       if (e != cudaSuccess) return e;
-      return gemm(a_plain ? static_cast<const uint16_t *>(a) : w.xpl, a_plain ? d_in : 0, a_nt, w.qpl, T, d_in, 1.0f,
-                  w.Z, 1, sk);
+      return gemm(w.xpl, a_nt, w.qpl, T, d_in, 1.0f, w.Z, 1, sk);
     };
     auto sketch = [&](const int *sk) -> cudaError_t {   // Y = A Q
       cudaError_t e;
       if (w.implicit) {   // A Q = a^T (a Q) / T
         if ((e = za(sk)) != cudaSuccess) return e;
         if ((e = launch_split_planes(L, w.Z, k, T, k, true, nt, w.zpl, sk)) != cudaSuccess) return e;
-        e = gemm(static_cast<const uint16_t *>(w.at), 0, a_nt, w.zpl, d_in, T, 1.0f / (float)T, w.Y, w.ksplit, sk);
+        e = gemm(static_cast<const uint16_t *>(w.at), a_nt, w.zpl, d_in, T, 1.0f / (float)T, w.Y, w.ksplit, sk);
       } else {
         if ((e = launch_split_planes(L, w.Q, k, d_in, k, true, nt, w.qpl, sk)) != cudaSuccess) return e;
-        e = gemm(w.apl, 0, nt, w.qpl, d_in, d_in, 1.0f, w.Y, w.ksplit, sk);
+        e = gemm(w.apl, nt, w.qpl, d_in, d_in, 1.0f, w.Y, w.ksplit, sk);
       }
       return e;
     };

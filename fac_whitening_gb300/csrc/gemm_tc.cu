@@ -13,10 +13,12 @@
 // never sums more than one 64-wide K chunk (24 MMAs at FP32 precision): the epilogue warps add
 // every chunk's accumulator into FP32 registers with round-to-nearest additions.
 //
-//   k_split_planes   FP32 source (rows x K, or K x rows when transposed) -> `nt` BF16 term
-//                    planes, each rows_pad x ldk (K-major rows, zero padded to a multiple of
-//                    128 rows and 64 columns), the layout a 128-byte-swizzled TMA box of
-//                    64 x 128 elements reads as a K-major tcgen05 operand.
+//   k_split_planes   FP32 or BF16 source (rows x K, or K x rows when transposed) -> `nt` BF16
+//                    term planes, each rows_pad x ldk (zero padded to a multiple of 128 rows
+//                    and 64 columns) and blocked: the 128-row x 64-K tile (r / 128, k / 64) is
+//                    16 KB of consecutive memory, rows of 64 K-major elements.  A
+//                    128-byte-swizzled TMA box of 64 x 128 (or 64 x 64) elements then reads one
+//                    contiguous run from DRAM and lands as a K-major tcgen05 operand.
 //   k_gemm_split     persistent over 128 x 128 tiles of C = alpha A B^T (A: M x K planes,
 //                    B: N x K planes; N <= 64 takes 128 x 64 tiles).  Warp 8 streams each
 //                    64-wide K chunk's term tiles with TMA (2 to 6 stages, as many as 220 KB of
@@ -58,7 +60,8 @@ struct GemmTcParams {
   int tiles_m, tiles_n, ntiles;   // ntiles counts work units: tiles (lower tiles only with
                                   // lower_tiles) times K slices
   int nta, ntb;            // term planes of A and B
-  int rows_a, rows_b;      // padded rows of one plane (multiples of 128)
+  int tiles_ra, tiles_rb;  // 128-row tiles of one plane of A and of B
+  int nch;                 // 64-wide K chunks of a plane row (ldk / 64)
   int nprod;               // products (pa[q], pb[q]) of the A and B terms, smallest first
   int8_t pa[kGMaxProducts], pb[kGMaxProducts];
   int a_lower, b_lower, lower_tiles;
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(256) k_split_planes(const Src *__restrict__ sr
   uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) tc::bf16_split3x2(tile[r][kb + 2 * q], tile[r][kb + 2 * q + 1], w1[q], w2[q], w3[q]);
-  const size_t off = (size_t)gr * ldk + k0 + kb;
+  const size_t off = ((size_t)(gr >> 7) * (ldk >> 6) + (k0 >> 6)) * 8192 + (size_t)(gr & 127) * 64 + kb;
   const size_t plane = (size_t)rows_pad * ldk;
   *reinterpret_cast<uint4 *>(planes + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
   if (nt > 1) *reinterpret_cast<uint4 *>(planes + plane + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
@@ -217,10 +220,14 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
           if (!(ok = wait(&empty[s], (uint32_t)(phase ^ 1)))) break;
           uint8_t *st = sm + (size_t)s * P.stage_bytes;
           tc::mbar_arrive_expect_tx(&full[s], (uint32_t)P.stage_bytes);
+          // blocked planes: the box of (plane p, row tile, chunk c) starts at row
+          // ((p * tiles + tile) * nch + c) * 128 of the 64-wide view
           for (int p = 0; p < P.nta; ++p)
-            tc::tma_load_2d(st + p * kGTile, &tmA, c * kGK, p * P.rows_a + tm * kGM, &full[s]);
+            tc::tma_load_2d(st + p * kGTile, &tmA, 0, ((p * P.tiles_ra + tm) * P.nch + c) * 128, &full[s]);
+          const int tb = (tn * BN) >> 7, sub = (tn * BN) & 127;
           for (int p = 0; p < P.ntb; ++p)
-            tc::tma_load_2d(st + P.nta * kGTile + p * (BN * 128), &tmB, c * kGK, p * P.rows_b + tn * BN, &full[s]);
+            tc::tma_load_2d(st + P.nta * kGTile + p * (BN * 128), &tmB, 0, ((p * P.tiles_rb + tb) * P.nch + c) * 128 + sub,
+                            &full[s]);
           ++g;
           if (++s == P.stages) {
             s = 0;
@@ -384,14 +391,13 @@ PFN_cuTensorMapEncodeTiled_v12000 gemm_encoder() {
   return fn;
 }
 
-// BF16 planes [rows_total][kdim] with a row stride of ld elements, boxes of 64 columns x
-// 128 rows, 128-byte swizzle; boxes beyond the rows or kdim read zeros.
-bool plane_map(CUtensorMap *m, const uint16_t *base, uint64_t rows_total, uint64_t kdim, uint64_t ld,
-               uint32_t box_rows = 128) {
+// Blocked BF16 planes viewed as rows of 64 elements (128 bytes): boxes of 64 x box_rows,
+// 128-byte swizzle.
+bool plane_map(CUtensorMap *m, const uint16_t *base, uint64_t rows_total, uint32_t box_rows = 128) {
   auto enc = gemm_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {kdim, rows_total};
-  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)kGK, rows_total};
+  const cuuint64_t strides[1] = {(cuuint64_t)kGK * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kGK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
@@ -456,19 +462,14 @@ __global__ void __launch_bounds__(256) k_sum_slices_tc(const float *__restrict__
 
 cudaError_t launch_gemm_planes(const Launch &L, const GemmPlanes &g) {
   const int ldk = pad_to(g.K, kGK);
-  // an operand given as a plain single-term matrix (a_ld > 0) has exactly M (N) rows of a_ld
-  // elements in memory; the padded planes have rows_pad rows of ldk
-  const int rows_a = g.a_ld ? g.M : pad_to(g.M, 128), rows_b = g.b_ld ? g.N : pad_to(g.N, 128);
+  const int rows_a = pad_to(g.M, 128), rows_b = pad_to(g.N, 128);
   if (g.nta < 1 || g.nta > 3 || g.ntb < 1 || g.ntb > 3 || g.ksplit < 1) return cudaErrorInvalidValue;
-  if ((g.a_ld && (g.nta != 1 || g.a_ld < g.K || g.a_ld % 8)) || (g.b_ld && (g.ntb != 1 || g.b_ld < g.K || g.b_ld % 8)))
-    return cudaErrorInvalidValue;
   if (g.lower_tiles && g.M != g.N) return cudaErrorInvalidValue;
   const int BN = (g.N <= 64 && !g.lower_tiles) ? 64 : 128;   // the tile's columns
   CUtensorMap tmA, tmB;
-  if (!plane_map(&tmA, g.pa, (uint64_t)g.nta * rows_a, (uint64_t)(g.a_ld ? g.K : ldk),
-                 (uint64_t)(g.a_ld ? g.a_ld : ldk)) ||
-      !plane_map(&tmB, g.pb, (uint64_t)g.ntb * rows_b, (uint64_t)(g.b_ld ? g.K : ldk),
-                 (uint64_t)(g.b_ld ? g.b_ld : ldk), (uint32_t)BN))
+  const uint64_t nchl = (uint64_t)(ldk / kGK);
+  if (!plane_map(&tmA, g.pa, (uint64_t)g.nta * rows_a * nchl) ||
+      !plane_map(&tmB, g.pb, (uint64_t)g.ntb * rows_b * nchl, (uint32_t)BN))
     return cudaErrorInvalidValue;
   GemmTcParams P;
   std::memset(&P, 0, sizeof(P));
@@ -485,8 +486,9 @@ cudaError_t launch_gemm_planes(const Launch &L, const GemmPlanes &g) {
   P.ntiles = tiles * g.ksplit;
   P.nta = g.nta;
   P.ntb = g.ntb;
-  P.rows_a = rows_a;
-  P.rows_b = rows_b;
+  P.tiles_ra = rows_a / 128;
+  P.tiles_rb = rows_b / 128;
+  P.nch = ldk / kGK;
   // the products x_i y_j kept: i + j <= 2 (0-based) at FP32 precision, i + j <= 1 otherwise;
   // smallest first
   const int maxsum = g.fp32 ? 2 : 1;

@@ -240,7 +240,8 @@ size_t gemm_tc_ws_bytes(int M, int N, int K, int nterms);
 size_t gemm_tc_plane_bytes(int rows, int K, int nterms);
 cudaError_t launch_gemm_tc(const Launch &L, const GemmArgs &g, int nt, void *ws);
 // The planes alone (rows x K, or the transpose of a K x rows source; rows padded to 128 and K
-// to 64 with zeros), and the product of two plane sets C = alpha A B^T (M x N, K):
+// to 64 with zeros; blocked: each 128-row x 64-K tile contiguous), and the product of two
+// plane sets C = alpha A B^T (M x N, K):
 //   nta / ntb   term planes of A and B (1..3; a BF16 source is its own single term);
 //   fp32        keep the products x_i y_j with i + j <= 2 (0-based), else i + j <= 1;
 //   a_lower / b_lower  row i of A (row j of B) is zero beyond k = i (j);
@@ -249,9 +250,7 @@ cudaError_t launch_gemm_tc(const Launch &L, const GemmArgs &g, int nt, void *ws)
 //               then summed in slice order;
 //   skip        nullable device flag: every launch does nothing while it is non-zero.
 struct GemmPlanes {
-  const uint16_t *pa = nullptr, *pb = nullptr;
-  int a_ld = 0, b_ld = 0;   // > 0: the operand is a plain BF16 matrix (one term, M or N rows of
-                            // this many elements, a multiple of 8) instead of padded planes
+  const uint16_t *pa = nullptr, *pb = nullptr;   // blocked term planes (launch_split_planes)
   int M = 0, N = 0, K = 0;
   int nta = 1, ntb = 1;
   bool fp32 = true;
