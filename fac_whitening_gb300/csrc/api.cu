@@ -49,6 +49,7 @@ struct CodecWs {
   float *split = nullptr;  // LOWRANK: tensor-core operand planes and counters (kernels.cuh)
   float *bpart = nullptr;  // LOWRANK, batched encode: kBatchWs x lr_batch_part_floats
   uint16_t *bplanes = nullptr;   // LOWRANK, batched encode: kBatchWs x 2 x d_out rows of 64 BF16
+  float *rdavg = nullptr;        // reduce and decode: the average, after the decode's workspace
   void *gplanes = nullptr;       // CHOL: BF16 term planes of the tensor-core GEMMs' operands
   int nsplit = 0;
   size_t bytes = 0;
@@ -70,6 +71,8 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
       w.bplanes = c.take<uint16_t>((size_t)kBatchWs * 2 * d_out * 64);
     }
   }
+  const bool rd = (op == GIFT_OP_REDUCE_DECODE);
+  if (rd) op = GIFT_OP_DECODE;   // the decode's workspace, then the average
   if (kind != GIFT_XF_IDENTITY) {
     if (op == GIFT_OP_DECODE || kind == GIFT_XF_CHOL_INPUT || kind == GIFT_XF_CHOL_TWO_SIDED)
       w.xbuf = c.take<float>(n);
@@ -81,6 +84,7 @@ CodecWs codec_layout(void *base, int sms, gift_op op, gift_xform kind, int d_out
       w.gplanes = c.take<uint8_t>(g);
     }
   }
+  if (rd && kind != GIFT_XF_IDENTITY) w.rdavg = c.take<float>(n);
   w.bytes = c.off;
   return w;
 }
@@ -371,7 +375,8 @@ size_t gift_workspace_bytes(const gift_ctx *ctx, gift_op op, gift_xform kind, gi
     if (kind == GIFT_XF_IDENTITY) return 0;
     return factor_layout(nullptr, ctx->sms, kind, d_out, d_in, T, ctx->sketch == 0).bytes;
   }
-  if (op != GIFT_OP_ENCODE && op != GIFT_OP_DECODE && op != GIFT_OP_AMAX) return (size_t)-1;
+  if (op != GIFT_OP_ENCODE && op != GIFT_OP_DECODE && op != GIFT_OP_AMAX && op != GIFT_OP_REDUCE_DECODE)
+    return (size_t)-1;
   return codec_layout(nullptr, ctx->sms, op, kind, d_out, d_in).bytes;
 }
 
@@ -1120,6 +1125,37 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
     CK(chol_unwhiten(L, f, X, d_out, d_in, W_out, w, prec));
   }
   return GIFT_OK;
+}
+
+gift_status gift_reduce_decode(gift_ctx *ctx, const gift_factor *f, int R, const void *const *codes,
+                               const void *const *scales, const float *const *tensor_scales, gift_format fmt,
+                               gift_scaling scaling, gift_precision prec, int d_out, int d_in, float *avg_out,
+                               float *W_out, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  if (!ctx || !codes || !W_out || R < 1 || R > kMaxReplicas || d_out <= 0 || d_in <= 0) return GIFT_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt) || !valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_F32 && !scales) return GIFT_ERR_INVALID_ARG;
+  if (fmt == GIFT_FMT_NVFP4 && (d_in % kNvGroup || !tensor_scales)) return GIFT_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r)
+    if (!codes[r] || (fmt != GIFT_FMT_F32 && !scales[r]) || (fmt == GIFT_FMT_NVFP4 && !tensor_scales[r]) ||
+        codes[r] == (const void *)W_out || codes[r] == (const void *)avg_out)
+      return GIFT_ERR_INVALID_ARG;
+  if (avg_out && avg_out == W_out) return GIFT_ERR_INVALID_ARG;
+  gift_status cs = check_factor(f, d_out, d_in);
+  if (cs != GIFT_OK) return cs;
+  const gift_xform kind = kind_of(f);
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_REDUCE_DECODE, kind, d_out, d_in);
+  if (need.bytes && (!ws || ws_bytes < need.bytes)) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_REDUCE_DECODE, kind, d_out, d_in);
+  // The average goes to avg_out or to the workspace's own buffer, back to back with the decode,
+  // which then reads it from L2 (a 1536 x 6144 average, 38 MB, stays resident).  The decode of
+  // an FP32 input uses the decode workspace's partials and planes, which this layout places
+  // before its average buffer.
+  float *X = avg_out ? avg_out : (kind == GIFT_XF_IDENTITY ? W_out : w.rdavg);
+  gift_status st = gift_replica_reduce(ctx, R, codes, scales, tensor_scales, fmt, scaling, d_out, d_in, X, d_status,
+                                       stream);
+  if (st != GIFT_OK || X == W_out) return st;
+  return gift_decode(ctx, f, X, 0, nullptr, nullptr, GIFT_FMT_F32, GIFT_SCALE_TENSOR, prec, d_out, d_in, W_out, ws,
+                     ws_bytes, d_status, stream);
 }
 
 gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int d_in, gift_format fmt,

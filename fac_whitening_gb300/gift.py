@@ -25,7 +25,7 @@ SCALING = {"tensor": 0, "block128": 1, "block512": 2}
 XFORM = {"identity": 0, "lowrank": 1, "chol_input": 2, "chol_two_sided": 3}
 PREC = {"fp32": 0, "tc": 1}
 DTYPE = {"f32": 0, "bf16": 1}
-OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3, "kfac_factor": 4}
+OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3, "kfac_factor": 4, "reduce_decode": 5}
 OPT_SUBSPACE_ITERS = 0
 OPT_BARRIER_WAIT = 1
 OPT_SKETCH = 2
@@ -84,6 +84,8 @@ def _declare(lib):
                                      _i, _i, _vp, _vp, _vp]),
         "gift_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
                              _vp, _vp]),
+        "gift_reduce_decode": (_i, [_vp, ctypes.POINTER(GiftFactor), _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                    ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]),
         "gift_boundary_hit_rate": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
         "gift_encode_lowrank_noalloc": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _vp, _vp, _vp, _vp,
                                              _vp, _vp]),
@@ -342,6 +344,17 @@ def gift_replica_reduce(ctx: Context, codes: Sequence, scales: Optional[Sequence
     _check(lib().gift_replica_reduce(ctx.handle, R, arr(codes), arr(scales), arr(tensor_scales), FMT[fmt],
                                      SCALING[scaling], d_out, d_in, _p(avg_out), _p(status), _stream(stream)),
            "gift_replica_reduce")
+
+
+def gift_reduce_decode(ctx: Context, f: Optional[Factor], codes: Sequence, scales: Optional[Sequence], fmt: str,
+                       scaling: str, d_out: int, d_in: int, W_out, avg_out=None, tensor_scales=None,
+                       prec: str = "fp32", ws=None, status=None, stream=None):
+    R = len(codes)
+    arr = lambda xs: (_vp * R)(*[_p(x) for x in xs]) if xs is not None else None  # noqa: E731
+    _check(lib().gift_reduce_decode(ctx.handle, _fptr(f), R, arr(codes), arr(scales), arr(tensor_scales), FMT[fmt],
+                                    SCALING[scaling], PREC[prec], d_out, d_in, _p(avg_out), _p(W_out), _p(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                    _stream(stream)), "gift_reduce_decode")
 
 
 def gift_decode(ctx: Context, f: Optional[Factor], inp, in_is_codes: bool, fmt: str, scaling: str, d_out: int,

@@ -144,7 +144,8 @@ typedef enum {
   GIFT_OP_ENCODE = 1,
   GIFT_OP_DECODE = 2,
   GIFT_OP_AMAX = 3,
-  GIFT_OP_KFAC_FACTOR = 4
+  GIFT_OP_KFAC_FACTOR = 4,
+  GIFT_OP_REDUCE_DECODE = 5
 } gift_op;
 
 /* Tunables for gift_set_option. */
@@ -348,6 +349,20 @@ gift_status gift_decode(gift_ctx *ctx, const gift_factor *f, const void *in, int
                         const void *scales, const float *tensor_scale, gift_format fmt,
                         gift_scaling scaling, gift_precision prec, int d_out, int d_in, float *W_out,
                         void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* Replica reduce and decode in one call ([notes] Algorithm 1: AllReduceSum, Dequantize,
+ * divide by N, then map back with the factor, eq. (14)): W_out = decode(average of the R
+ * replicas' codes).  It enqueues gift_replica_reduce into avg_out (or into the workspace) and
+ * then gift_decode of that average, back to back, so that the decode reads the average from
+ * L2; the results are those two calls' (the average bit for bit).
+ *  codes, scales, tensor_scales : as gift_replica_reduce.
+ *  avg_out : device, nullable, d_out x d_in FP32: receives the average.
+ *  W_out   : device, d_out x d_in FP32.  Must alias neither the codes nor avg_out.
+ *  ws      : gift_workspace_bytes(GIFT_OP_REDUCE_DECODE, ...) bytes.  1 <= R <= 64. */
+gift_status gift_reduce_decode(gift_ctx *ctx, const gift_factor *f, int R, const void *const *codes,
+                               const void *const *scales, const float *const *tensor_scales, gift_format fmt,
+                               gift_scaling scaling, gift_precision prec, int d_out, int d_in, float *avg_out,
+                               float *W_out, void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
 
 /* Boundary-hit profiler ([notes] simplification 3: encode the flattened gradient with the
  * scale that would be used and count codes on the upper or lower boundary of the FP8
