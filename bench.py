@@ -50,7 +50,8 @@ def parse():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="gift", choices=["gift", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-configs", action="store_true", help="skip the other configurations' measurements")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=13, help="geometry-aware layers (13 in the workload)")
@@ -222,7 +223,7 @@ def run_reference(args):
     if rank != 0:
         return
     # each step is a bounded sample, so that --steps K --warmup W ends within a few minutes
-    sample = make_oracle_sample(rows=256)
+    sample = make_oracle_sample(rows=512)   # about 2 s per step on one core
     dt, threads = time_oracle(sample, args.steps, args.warmup)
     value = sample["bytes"] / dt / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
@@ -544,6 +545,15 @@ def main_gift(args):
     except Exception as ex:   # a measurement, never a reason to lose the bench line
         fid = {"error": str(ex)[:200]}
 
+    # ---- the other configurations and the fidelity per format ---------------------------
+    configs = None
+    if not args.no_configs and rank == 0:
+        try:
+            configs = other_configs(G, ctx, dev, hbm_peak, bf16_peak, peak_kind,
+                                    gl0=gl[0]["W"] if gl else None, f0=factors[0] if factors else None)
+        except Exception as ex:   # a measurement, never a reason to lose the bench line
+            configs = {"error": str(ex)[:200]}
+
     # ---- roofline of the dominant kernel ----------------------------------------------
     # The dominant group is the Euclidean shared-scale encode (one cooperative launch per
     # tensor: amax of its R replicas, grid barrier, pack) or the rank-r encode (one
@@ -588,7 +598,7 @@ def main_gift(args):
     # ---- CPU baseline (oracle on a bounded sample) --------------------------------------
     cpu = None
     if not args.no_cpu_baseline and rank == 0:
-        sample = make_oracle_sample(rows=768)   # about 15 s of single-core work
+        sample = make_oracle_sample(rows=1536)   # the whole layer: about 7 s of single-core work
         dt, threads = time_oracle(sample, 1)
         cpu = cpu_baseline_entry(sample, dt, threads, omp=time_oracle(sample, 1, warmup=1, openmp=True))
 
@@ -604,7 +614,7 @@ def main_gift(args):
                            "parallelism": f"replicas x{world}", "streams_per_stage": nstr},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": kernels_per_step * args.steps, "stages": stages, "fidelity": fid,
-                "factor_syrk": kfac,
+                "factor_syrk": kfac, "configs": configs,
                 "factor_refresh": {p: {"ms_per_layer": ms_, "syrk_tflops": syrk_flops / (ms_ * 1e-3) / 1e12}
                                    for p, ms_ in refresh.items()} | {
                                    "note": "whole refresh (SYRK + rank-32 subspace iteration + Jacobi) per layer, "
@@ -614,6 +624,256 @@ def main_gift(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------------------------------
+# The other configurations and the fidelity per format (after the timed region)
+# --------------------------------------------------------------------------------------
+def time_cold(fn, reps=5):
+    """Mean ms of fn() over reps, each run after a 256 MB write (L2 flushed), CUDA events on
+    the current stream."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / reps
+
+
+def codec_pass(G, ctx, f, Ws, fmt, scaling, ws_enc, ws_dec, st, prec="fp32"):
+    """Buffers and closures for one layer's encode (its R replicas), reduce and decode."""
+    import torch
+    d_out, d_in = Ws[0].shape
+    R = len(Ws)
+    cb, sc = G.gift_code_sizes(fmt, scaling, d_out, d_in)
+    codes = [torch.empty(cb, dtype=torch.uint8, device="cuda") for _ in range(R)]
+    sdt = torch.uint8 if fmt == "nvfp4" else torch.float32
+    scales = [torch.empty(sc, dtype=sdt, device="cuda") for _ in range(R)]
+    tsc = [torch.empty(1, device="cuda") for _ in range(R)] if fmt == "nvfp4" else None
+    avg = torch.empty(d_out, d_in, device="cuda")
+    out = torch.empty(d_out, d_in, device="cuda")
+    P = {"codes": codes, "scales": scales, "tsc": tsc, "avg": avg, "out": out}
+    P["encode"] = lambda: G.gift_encode_replicas(ctx, f, Ws, fmt, scaling, codes, scales=scales, tensor_scales=tsc,
+                                                  prec=prec, ws=ws_enc, status=st)
+    P["reduce"] = lambda: G.gift_replica_reduce(ctx, codes, scales, fmt, scaling, d_out, d_in, avg,
+                                                tensor_scales=tsc, status=st)
+    P["decode"] = lambda: G.gift_decode(ctx, f, avg, False, "f32", "tensor", d_out, d_in, out, prec=prec,
+                                        ws=ws_dec, status=st)
+    return P
+
+
+def measure_codec(G, ctx, f, Ws, fmt, scaling, st, hbm_peak, prec="fp32", reps=5):
+    """GB/s of FP32 gradient (4 bytes per element of every replica) and the fraction of the HBM
+    peak on the algorithmic bytes of each stage: encode 4 + code bytes, reduce R x code bytes
+    + 4, decode 8 per element."""
+    import torch
+    d_out, d_in = Ws[0].shape
+    kind = "identity" if f is None else f.kind
+    R = len(Ws)
+    n = d_out * d_in
+    cbytes = {"nvfp4": 0.5 + 1 / 16, "f32": 4}.get(fmt, 1.0)
+    ws_enc = torch.zeros(max(G.gift_workspace_bytes(ctx, "encode", kind, fmt, scaling, d_out, d_in), 256),
+                         dtype=torch.uint8, device="cuda")
+    ws_dec = torch.zeros(max(G.gift_workspace_bytes(ctx, "decode", kind, "f32", "tensor", d_out, d_in), 256),
+                         dtype=torch.uint8, device="cuda")
+    P = codec_pass(G, ctx, f, Ws, fmt, scaling, ws_enc, ws_dec, st, prec)
+    res = {}
+    alg = {"encode": R * n * (4 + cbytes), "reduce": n * (R * cbytes + 4), "decode": n * 8}
+    for stage in ("encode", "reduce", "decode"):
+        ms = time_cold(P[stage], reps)
+        res[stage] = {"us": ms * 1e3, "GB/s_gradient": (R if stage == "encode" else 1) * 4 * n / (ms * 1e-3) / 1e9,
+                      "hbm_frac": alg[stage] / (ms * 1e-3) / 1e9 / hbm_peak}
+    return res, P
+
+
+def fidelity_gift_vs_euclid(G, ctx, f, Ws, fmt, st):
+    """RelL2, Cos, MaxErr, MSE (eq. (15)) of the decoded layer against the FP32 mean of its
+    replicas: GIFT (the factor's transform, per-replica scales) and the Euclidean path (identity,
+    the replicas' shared scale)."""
+    import torch
+    d_out, d_in = Ws[0].shape
+    kind = f.kind
+    gbar = torch.zeros(d_out, d_in, dtype=torch.float64, device="cuda")
+    for W in Ws:
+        gbar += W.double()
+    gbar /= len(Ws)
+    ws_enc = torch.zeros(G.gift_workspace_bytes(ctx, "encode", kind, fmt, "tensor", d_out, d_in),
+                         dtype=torch.uint8, device="cuda")
+    ws_dec = torch.zeros(G.gift_workspace_bytes(ctx, "decode", kind, "f32", "tensor", d_out, d_in),
+                         dtype=torch.uint8, device="cuda")
+    P = codec_pass(G, ctx, f, Ws, fmt, "tensor", ws_enc, ws_dec, st)
+    P["encode"]()
+    P["reduce"]()
+    P["decode"]()
+    E = codec_pass(G, ctx, None, Ws, fmt, "tensor", ws_enc, ws_dec, st)
+    G.gift_encode_replicas_shared(ctx, None, Ws, fmt, "tensor", E["codes"], E["scales"], tensor_scales=E["tsc"],
+                                  ws=ws_enc, status=st)
+    E["reduce"]()
+    torch.cuda.synchronize()
+    return {"gift": fidelity_stats(P["out"], gbar), "euclid": fidelity_stats(E["avg"], gbar)}
+
+
+def other_configs(G, ctx, dev, hbm_peak, bf16_peak, peak_kind, gl0=None, f0=None):
+    """One line per configuration besides the timed 600M-like step: codec GB/s per stage and
+    format, the factor refresh, and the fidelity per format, GIFT against Euclidean."""
+    import torch
+    from fac_whitening_gb300 import synth
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+
+    def refresh_ms(kind, a, d_out, delta=None, prec="fp32"):
+        d_in = a.shape[1]
+        f = G.Factor.empty(kind, d_out, d_in, 32, device=dev)
+        w = torch.zeros(G.gift_workspace_bytes(ctx, "factor_update", kind, FMT, "tensor", d_out, d_in, a.shape[0]),
+                        dtype=torch.uint8, device=dev)
+        ms = time_cold(lambda: G.gift_factor_update(ctx, f, a, delta=delta, seed=3, prec=prec, ws=w, status=st), 2)
+        del w
+        return f, ms
+
+    # ---- tiny single layer: 64 x 256, T = 512 FP32, rank 32, E4M3, R = 4 -----------------
+    try:
+        wl = synth.tiny_workload()
+        spec = wl.layers[0]
+        Ws, a = synth.layer_inputs(spec, wl.config, 0, wl.R, device=dev)
+        f, fms = refresh_ms("lowrank", a, spec.d_out)
+        codec, _ = measure_codec(G, ctx, f, Ws, "e4m3", "tensor", st, hbm_peak)
+        out["tiny_64x256"] = {"factor_refresh_ms": fms, "codec_e4m3": codec,
+                              "fidelity_e4m3": fidelity_gift_vs_euclid(G, ctx, f, Ws, "e4m3", st)}
+    except Exception as ex:
+        out["tiny_64x256"] = {"error": str(ex)[:200]}
+
+    # ---- 300M-like fc2: 1024 x 4096, T = 8192 BF16, R = 8; every transform --------------
+    try:
+        wl = synth.llama300m_fc2_workload()
+        spec = wl.layers[0]
+        Ws, a = synth.layer_inputs(spec, wl.config, 0, wl.R, device=dev)
+        delta = synth.delta_for_layer(spec, wl.config, 0, device=dev)
+        res = {}
+        for kind in ("chol_two_sided", "chol_input", "lowrank"):
+            f, fms = refresh_ms(kind, a, spec.d_out, delta=delta if kind == "chol_two_sided" else None)
+            codec, _ = measure_codec(G, ctx, f, Ws, "e4m3", "tensor", st, hbm_peak)
+            entry = {"factor_refresh_ms": fms, "codec_e4m3": codec,
+                     "fidelity_e4m3": fidelity_gift_vs_euclid(G, ctx, f, Ws, "e4m3", st)}
+            if kind != "lowrank":   # triangular products W L^-T (d_in^2 d_out) and L_G^-1 X (d_out^2 d_in)
+                fl = spec.d_out * spec.d_in * spec.d_in + (spec.d_out ** 2 * spec.d_in if kind == "chol_two_sided" else 0)
+                entry["transform_tflops_fp32_equivalent"] = fl / (codec["encode"]["us"] * 1e-6 / wl.R) / 1e12
+            res[kind] = entry
+            del f
+        codec, _ = measure_codec(G, ctx, None, Ws, "e4m3", "tensor", st, hbm_peak)
+        res["identity"] = {"codec_e4m3": codec}
+        out["llama300m_fc2_1024x4096"] = res
+        del Ws, a, delta
+    except Exception as ex:
+        out["llama300m_fc2_1024x4096"] = {"error": str(ex)[:200]}
+    torch.cuda.empty_cache()
+
+    # ---- 600M-like fc2 layer 0: fidelity per format ------------------------------------
+    if gl0 is not None and f0 is not None:
+        try:
+            out["llama600m_fc2_fidelity"] = {fmt: fidelity_gift_vs_euclid(G, ctx, f0, gl0, fmt, st)
+                                             for fmt in ("e4m3", "e5m2", "nvfp4")}
+            codec, _ = measure_codec(G, ctx, f0, gl0, "nvfp4", "tensor", st, hbm_peak)
+            out["llama600m_fc2_codec_nvfp4"] = codec
+            codec, _ = measure_codec(G, ctx, f0, gl0, "e5m2", "tensor", st, hbm_peak)
+            out["llama600m_fc2_codec_e5m2"] = codec
+        except Exception as ex:
+            out["llama600m_fc2_fidelity"] = {"error": str(ex)[:200]}
+
+    # ---- profiler + per-block scaling: 48 heavy-tailed gradients -----------------------
+    try:
+        wl = synth.profiler_workload()
+        grads = [synth.layer_inputs(sp, wl.config, i, 1, device=dev)[0][0] for i, sp in enumerate(wl.layers)]
+        n_all = sum(g.numel() for g in grads)
+        res = {}
+        counts = torch.zeros(len(grads), 3, dtype=torch.int64, device=dev)
+        wsa = torch.zeros(max(G.gift_workspace_bytes(ctx, "amax", "identity", "e4m3", "tensor", 6144, 6144), 256),
+                          dtype=torch.uint8, device=dev)
+        for fmt in ("e4m3", "e5m2"):
+            def hits():
+                counts.zero_()
+                for i, g in enumerate(grads):
+                    G.gift_boundary_hit_rate(ctx, g, fmt, "tensor", counts[i], ws=wsa, status=st)
+            ms = time_cold(hits, 3)
+            res[f"hit_rate_{fmt}"] = {"us_all_48": ms * 1e3, "GB/s_gradient": 4 * n_all / (ms * 1e-3) / 1e9,
+                                      "hbm_frac": 4 * n_all / (ms * 1e-3) / 1e9 / hbm_peak}
+        counts.zero_()   # the selection uses the E4M3 counts
+        for i, g in enumerate(grads):
+            G.gift_boundary_hit_rate(ctx, g, "e4m3", "tensor", counts[i], ws=wsa, status=st)
+        order, _, k = G.gift_select_fragile(counts.cpu().numpy().astype("uint64"), 13)
+        sel = [grads[i] for i in order[:k]]
+        # the selected layers encoded with 128 x 128 block scales after a rank-32 whitening
+        fac = {}
+        for g in sel:
+            if g.shape[1] not in fac:
+                q, _ = torch.linalg.qr(torch.randn(g.shape[1], 32, device=dev))
+                fac[g.shape[1]] = (q.contiguous(), torch.linspace(40, 1, 32, device=dev))
+        n_sel = sum(g.numel() for g in sel)
+        bufs = []
+        for g in sel:
+            U, mu = fac[g.shape[1]]
+            f = G.Factor("lowrank", g.shape[0], g.shape[1], 32, U=U, mu=mu, sigma=torch.tensor([0.1], device=dev))
+            cb, sc = G.gift_code_sizes("e4m3", "block128", *g.shape)
+            w = torch.zeros(G.gift_workspace_bytes(ctx, "encode", "lowrank", "e4m3", "block128", *g.shape),
+                            dtype=torch.uint8, device=dev)
+            bufs.append((f, g, torch.empty(cb, dtype=torch.uint8, device=dev), torch.empty(sc, device=dev), w))
+
+        def enc13():
+            for f, g, c, s_, w in bufs:
+                G.gift_encode(ctx, f, g, "e4m3", "block128", c, s_, ws=w, status=st)
+        ms = time_cold(enc13, 3)
+        res["top13_block128_rank32_encode"] = {"us_all_13": ms * 1e3, "GB/s_gradient": 4 * n_sel / (ms * 1e-3) / 1e9,
+                                               "hbm_frac": 5 * n_sel / (ms * 1e-3) / 1e9 / hbm_peak,
+                                               "selected": [int(i) for i in order[:k]]}
+        out["profiler_48"] = res
+        del grads, sel, bufs
+    except Exception as ex:
+        out["profiler_48"] = {"error": str(ex)[:200]}
+    torch.cuda.empty_cache()
+
+    # ---- large stress: one fc2-like 4096 x 16384 layer, R = 16, E4M3 and NVFP4 ----------
+    try:
+        D_OUT, D_IN, R = 4096, 16384, 16
+        gen = torch.Generator(device=dev).manual_seed(62)
+        U, _ = torch.linalg.qr(torch.randn(D_IN, 32, generator=gen, device=dev))
+        mu = (1.0 / torch.arange(1, 33, device=dev, dtype=torch.float32))
+        mu[torch.randperm(32, generator=torch.Generator().manual_seed(5))[:8].to(dev)] *= 100.0
+        mu = torch.sort(mu, descending=True).values
+        f = G.Factor("lowrank", D_OUT, D_IN, 32, U=U.contiguous(), mu=mu, sigma=torch.tensor([0.01], device=dev))
+        Ws = []
+        for _ in range(R):
+            W = torch.randn(D_OUT, D_IN, generator=gen, device=dev) * 0.1
+            W += (torch.randn(D_OUT, 32, generator=gen, device=dev) * 3.0) @ U.T
+            Ws.append(W.contiguous())
+        res = {}
+        for fmt in ("e4m3", "nvfp4"):
+            codec, P = measure_codec(G, ctx, f, Ws, fmt, "tensor", st, hbm_peak, reps=3)
+            res[f"codec_{fmt}"] = codec
+            del P
+            res[f"fidelity_{fmt}"] = fidelity_gift_vs_euclid(G, ctx, f, Ws, fmt, st)
+        # the factor refresh at this size: T = 32768 BF16 activations with the spectrum i^-1
+        # and 8 spikes (coordinate eigenvectors: the sketch's convergence is the same)
+        del Ws
+        torch.cuda.empty_cache()
+        s = synth.spectrum_power_law(D_IN, 1.0)
+        s[synth.spike_indices(D_IN, 8, 5)] *= 10.0
+        a = (torch.randn(32768, D_IN, generator=gen, device=dev) * s.to(dev, torch.float32)).to(torch.bfloat16)
+        _, fms = refresh_ms("lowrank", a, D_OUT)
+        res["factor_refresh_ms"] = fms
+        out["stress_4096x16384_R16"] = res
+        del a, f
+    except Exception as ex:
+        out["stress_4096x16384_R16"] = {"error": str(ex)[:200]}
+    torch.cuda.empty_cache()
+    out["device_status"] = int(st.item())
+    return out
 
 
 def near_gpu_cpus(device):
