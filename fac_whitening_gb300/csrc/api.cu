@@ -155,17 +155,20 @@ FactorWs factor_layout(void *base, int sms, gift_xform kind, int d_out, int d_in
     w.ev = c.take<double>(64);
     w.tr = c.take<double>(1);
     w.sq = c.take<double>((size_t)trace_partials(sms));
-    if (w.k == 64 && d_in > 64 && T > 0) {
+    if (w.k == 64 && d_in > 64) {
+      // T == 0: the factor of a given A (explicit sketch, no activations)
       const size_t rows = (size_t)(d_in + 127) / 128 * 128, ldk = (size_t)(d_in + 63) / 64 * 64;
       const size_t rows_t = (size_t)(T + 127) / 128 * 128, ldt = (size_t)(T + 63) / 64 * 64;
-      w.implicit = implicit;
-      if (!implicit) w.apl = c.take<uint16_t>(3 * rows * ldk);
+      w.implicit = implicit && T > 0;
+      if (!w.implicit) w.apl = c.take<uint16_t>(3 * rows * ldk);
       w.qpl = c.take<uint16_t>(3 * 128 * ldk);
-      w.xpl = c.take<uint16_t>(3 * rows_t * ldk);   // the activations as term planes
-      w.zpl = c.take<uint16_t>(3 * 128 * ldt);
-      w.Z = c.take<float>((size_t)T * 64);
+      if (T > 0) {
+        w.xpl = c.take<uint16_t>(3 * rows_t * ldk);   // the activations as term planes
+        w.zpl = c.take<uint16_t>(3 * 128 * ldt);
+        w.Z = c.take<float>((size_t)T * 64);
+      }
       // split-K of the d-row products (A Q over K = d, or a^T Z over K = T)
-      const int tiles_m = (int)(rows / 128), nch = (int)((implicit ? ldt : ldk) / 64);
+      const int tiles_m = (int)(rows / 128), nch = (int)((w.implicit ? ldt : ldk) / 64);
       w.ksplit = std::max(1, std::min(sms / tiles_m, nch));
       w.parts = c.take<float>(gemm_tc_parts_floats(d_in, 64, w.ksplit));
       w.B32 = c.take<float>(64 * 64);
@@ -484,19 +487,24 @@ gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int 
   return GIFT_OK;
 }
 
-gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
-                               const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
-                               void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
-  if (!ctx || !f || !a || T < 1) return GIFT_ERR_INVALID_ARG;
+// The factor refresh from activations (a, T > 0; delta for the two-sided kind) or from given
+// K-FAC factors (A_in, and G_in for the two-sided kind; T = 0).
+static gift_status factor_update_impl(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
+                                      const void *delta, gift_dtype d_dt, const float *A_in, const float *G_in,
+                                      uint64_t seed, gift_precision prec, void *ws, size_t ws_bytes, int *d_status,
+                                      cudaStream_t stream) {
+  if (!ctx || !f) return GIFT_ERR_INVALID_ARG;
+  if (A_in ? (a || T != 0) : (!a || T < 1)) return GIFT_ERR_INVALID_ARG;
   if (prec != GIFT_PREC_FP32 && prec != GIFT_PREC_TC) return GIFT_ERR_INVALID_ARG;
   const int d_in = f->d_in, d_out = f->d_out;
   if (d_in <= 0 || d_out <= 0) return GIFT_ERR_INVALID_ARG;
-  if (a_dt != GIFT_DT_F32 && a_dt != GIFT_DT_BF16) return GIFT_ERR_INVALID_ARG;
+  if (!A_in && a_dt != GIFT_DT_F32 && a_dt != GIFT_DT_BF16) return GIFT_ERR_INVALID_ARG;
   if (f->kind == GIFT_XF_IDENTITY || !valid_kind(f->kind)) return GIFT_ERR_INVALID_ARG;
   gift_status cs = check_factor(f, d_out, d_in);
   if (cs != GIFT_OK) return cs;
-  if (f->kind == GIFT_XF_CHOL_TWO_SIDED && (!delta || (d_dt != GIFT_DT_F32 && d_dt != GIFT_DT_BF16)))
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED && !A_in && (!delta || (d_dt != GIFT_DT_F32 && d_dt != GIFT_DT_BF16)))
     return GIFT_ERR_INVALID_ARG;
+  if (f->kind == GIFT_XF_CHOL_TWO_SIDED && A_in && !G_in) return GIFT_ERR_INVALID_ARG;
   const FactorWs need = factor_layout(nullptr, ctx->sms, f->kind, d_out, d_in, T, ctx->sketch == 0);
   if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
   const FactorWs w = factor_layout(ws, ctx->sms, f->kind, d_out, d_in, T, ctx->sketch == 0);
@@ -506,7 +514,9 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
   auto syrk = [&](const void *x, bool bf16, int d, float *out) -> cudaError_t {
     return kfac_syrk(L, x, bf16, T, d, prec, w.at, w.at_bytes, out);
   };
-  if (!(f->kind == GIFT_XF_LOWRANK && w.qpl)) CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
+  // the input-side factor: formed from the activations, or the caller's
+  const float *A = A_in ? A_in : w.A;
+  if (!A_in && !(f->kind == GIFT_XF_LOWRANK && w.qpl)) CK(syrk(a, a_dt == GIFT_DT_BF16, d_in, w.A));
 
   if (f->kind == GIFT_XF_LOWRANK && w.qpl) {
     // FP32 subspace iteration with Rayleigh-Ritz steps, the products on the tensor cores
@@ -517,8 +527,10 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
     const int *skip = w.flag;
     // the activations as the A operand of Z = a Q (M = T, K = d_in): one term for BF16, split
     // into terms for FP32
-    if (bf16) CK(launch_split_planes_bf16(L, a, T, d_in, d_in, false, w.xpl));
-    else CK(launch_split_planes(L, static_cast<const float *>(a), T, d_in, d_in, false, nt, w.xpl));
+    if (a) {
+      if (bf16) CK(launch_split_planes_bf16(L, a, T, d_in, d_in, false, w.xpl));
+      else CK(launch_split_planes(L, static_cast<const float *>(a), T, d_in, d_in, false, nt, w.xpl));
+    }
     const int a_nt = bf16 ? 1 : nt;
     if (w.implicit) {
       // a^T as the A operand of Y = a^T Z / T (M = d_in, K = T), in the K-FAC workspace
@@ -528,9 +540,9 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
       if (aligned16(a)) CK(launch_trace_acts32(L, a, bf16, T, d_in, w.sq, trace_partials(ctx->sms), w.tr));
       else CK(launch_trace_from_activations(L, a, bf16, T, d_in, w.sq, w.tr));
     } else {
-      CK(syrk(a, bf16, d_in, w.A));
-      CK(launch_trace_diag(L, w.A, d_in, w.tr));
-      CK(launch_split_planes(L, w.A, d_in, d_in, d_in, false, nt, w.apl));
+      if (!A_in) CK(syrk(a, bf16, d_in, w.A));
+      CK(launch_trace_diag(L, A, d_in, w.tr));
+      CK(launch_split_planes(L, A, d_in, d_in, d_in, false, nt, w.apl));
     }
     CK(cudaMemsetAsync(w.flag, 0, sizeof(int), stream));
     auto orth = [&](float *Y, const int *sk) -> cudaError_t {   // Q = Y R^-1, twice (CholQR2)
@@ -599,9 +611,15 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
       CK(orth(w.Y, skip));
     }
     // final Rayleigh-Ritz step from the activations: B = Q^T A Q = (a Q)^T (a Q) / T, a Gram
-    // matrix (no cancellation between large and small eigenvalues), solved to convergence
-    CK(za(nullptr));
-    CK(launch_gram_tall(L, w.Z, w.Z, T, k, w.gparts, w.B32, true, nullptr, 1.0f / (float)T));
+    // matrix (no cancellation between large and small eigenvalues), solved to convergence;
+    // from a given A, B = Q^T (A Q)
+    if (a) {
+      CK(za(nullptr));
+      CK(launch_gram_tall(L, w.Z, w.Z, T, k, w.gparts, w.B32, true, nullptr, 1.0f / (float)T));
+    } else {
+      CK(sketch(nullptr));
+      CK(launch_gram_tall(L, w.Q, w.Y, d_in, k, w.gparts, w.B32, true, nullptr));
+    }
     CK(launch_jacobi32(L, w.B32, k, w.th, w.V32, 40, true, nullptr));
     CK(launch_f32_to_f64(L, w.V32, w.V, (size_t)k * k));
     CK(launch_f32_to_f64(L, w.th, w.ev, (size_t)k));
@@ -612,7 +630,8 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
 
   if (f->kind == GIFT_XF_LOWRANK) {
     const int k = w.k;
-    CK(launch_trace_from_activations(L, a, a_dt == GIFT_DT_BF16, T, d_in, w.sq, w.tr));
+    if (a) CK(launch_trace_from_activations(L, a, a_dt == GIFT_DT_BF16, T, d_in, w.sq, w.tr));
+    else CK(launch_trace_diag(L, A, d_in, w.tr));
     auto cholqr = [&](const float *in, float *out) -> cudaError_t {
       DgemmArgs g{};
       g.A = in; g.B = in; g.C = w.Gp;
@@ -632,13 +651,13 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
     };
     auto aq = [&]() -> cudaError_t {   // Y = A Q
       GemmArgs g{};
-      g.A = w.A; g.B = w.Q; g.C = w.Y;
+      g.A = A; g.B = w.Q; g.C = w.Y;
       g.M = d_in; g.N = k; g.K = d_in; g.lda = d_in; g.ldb = k; g.ldc = k; g.alpha = 1.0f;
       return launch_sgemm_splitk(L, g, w.yparts, w.ysplits);
     };
     if (k == d_in) {
       CK(launch_eye(L, w.Q, k));
-      CK(launch_f32_to_f64(L, w.A, w.G, (size_t)k * k));
+      CK(launch_f32_to_f64(L, A, w.G, (size_t)k * k));
     } else {
       CK(launch_philox_gaussian(L, w.Y, (size_t)d_in * k, seed));
       CK(cholqr(w.Y, w.Q));
@@ -665,19 +684,35 @@ gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gif
 
   // Cholesky variants
   const size_t nn = (size_t)d_in * d_in;
-  CK(launch_f32_to_f64(L, w.A, w.A64, nn));
+  CK(launch_f32_to_f64(L, A, w.A64, nn));
   CK(launch_chol_inv(L, w.A64, w.Ai64, d_in, w.work));
   CK(launch_f64_to_f32(L, w.A64, f->LA, nn, true, d_in));
   CK(launch_f64_to_f32(L, w.Ai64, f->LAinv, nn, true, d_in));
   if (f->kind == GIFT_XF_CHOL_TWO_SIDED) {
     const size_t mm = (size_t)d_out * d_out;
-    CK(syrk(delta, d_dt == GIFT_DT_BF16, d_out, w.Gf));
-    CK(launch_f32_to_f64(L, w.Gf, w.G64, mm));
+    if (!G_in) CK(syrk(delta, d_dt == GIFT_DT_BF16, d_out, w.Gf));
+    CK(launch_f32_to_f64(L, G_in ? G_in : w.Gf, w.G64, mm));
     CK(launch_chol_inv(L, w.G64, w.Gi64, d_out, w.work));
     CK(launch_f64_to_f32(L, w.G64, f->LG, mm, true, d_out));
     CK(launch_f64_to_f32(L, w.Gi64, f->LGinv, mm, true, d_out));
   }
   return GIFT_OK;
+}
+
+gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
+                               const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
+                               void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream) {
+  if (!a || T < 1) return GIFT_ERR_INVALID_ARG;
+  return factor_update_impl(ctx, f, a, a_dt, T, delta, d_dt, nullptr, nullptr, seed, prec, ws, ws_bytes, d_status,
+                            stream);
+}
+
+gift_status gift_factor_update_from_kfac(gift_ctx *ctx, gift_factor *f, const float *A, const float *G,
+                                         uint64_t seed, gift_precision prec, void *ws, size_t ws_bytes,
+                                         int *d_status, cudaStream_t stream) {
+  if (!A) return GIFT_ERR_INVALID_ARG;
+  return factor_update_impl(ctx, f, nullptr, GIFT_DT_F32, 0, nullptr, GIFT_DT_F32, A, G, seed, prec, ws, ws_bytes,
+                            d_status, stream);
 }
 
 // -----------------------------------------------------------------------------------------

@@ -65,6 +65,8 @@ def _declare(lib):
         "gift_code_sizes": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
         "gift_factor_update": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _vp, _i, ctypes.c_uint64, _i,
                                     _vp, _sz, _vp, _vp]),
+        "gift_factor_update_from_kfac": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _vp, ctypes.c_uint64, _i, _vp,
+                                              _sz, _vp, _vp]),
         "gift_kfac_factor": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
         "gift_factor_planes_bytes": (_sz, [_i]),
         "gift_factor_prepare": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp]),
@@ -264,6 +266,14 @@ def gift_factor_update(ctx: Context, f: Factor, a, delta=None, seed: int = 0, pr
     _check(lib().gift_factor_update(ctx.handle, ctypes.byref(st), _p(a), a_dt, a.shape[0], _p(delta), d_dt,
                                     seed, PREC[prec], _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                     _p(status), _stream(stream)), "gift_factor_update")
+
+
+def gift_factor_update_from_kfac(ctx: Context, f: Factor, A, G=None, seed: int = 0, prec: str = "fp32", ws=None,
+                                 status=None, stream=None):
+    st = f.c_struct()
+    _check(lib().gift_factor_update_from_kfac(ctx.handle, ctypes.byref(st), _p(A), _p(G), seed, PREC[prec], _p(ws),
+                                              0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                              _stream(stream)), "gift_factor_update_from_kfac")
 
 
 def gift_factor_prepare(ctx: Context, f: Factor, stream=None):

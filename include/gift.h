@@ -193,23 +193,50 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
  *  delta  : device, T x d_out output gradients of type d_dt (CHOL_TWO_SIDED only, else NULL).
  *  f      : f->kind selects the factor; its buffers receive the result.
  *  LOWRANK: randomised block subspace iteration on A with a seeded Gaussian start of
- *           k = min(64, d_in) columns (Philox4x32-10 from `seed`), GIFT_OPT_SUBSPACE_ITERS
- *           power steps with CholQR2 re-orthonormalisation, Rayleigh-Ritz and a one-CTA
- *           Jacobi eigensolve; U = Q V[:, :rank]; sigma = (tr A - sum mu) / (d_in - rank)
- *           (sigma = 1 when rank == d_in).  d_status: NOT_PD when sigma or a mu is <= 0,
- *           NOT_CONVERGED when the Jacobi sweeps do not converge.
+ *           k = min(64, d_in) columns (Philox4x32-10 from `seed`).  For d_in > 64 it runs
+ *           in FP32 with every product on the tensor cores (FP32 operands split exactly
+ *           into BF16 terms, one fresh FP32 accumulator per 64-deep chunk): each power step
+ *           forms Y = A Q (by default as a^T (a Q) / T, A never formed; GIFT_OPT_SKETCH
+ *           selects the explicit product) and re-orthonormalises Q by CholQR2 with
+ *           compensated FP32 Gram sums; Rayleigh-Ritz steps (FP32 parallel Jacobi) rotate
+ *           Q on the first two steps and every fourth, and stop the iteration once the top
+ *           `rank` Ritz values move by less than a quarter ulp (at most
+ *           GIFT_OPT_SUBSPACE_ITERS steps, default 16).  The last Rayleigh-Ritz step takes
+ *           Q^T A Q as the Gram matrix of a Q.  For d_in <= 64 the Gram, Cholesky and
+ *           eigensolve run in FP64 on A itself.  U = Q V[:, :rank]; sigma =
+ *           (tr A - sum mu) / (d_in - rank) (sigma = 1 when rank == d_in).  d_status:
+ *           NOT_PD when sigma or a mu is <= 0, NOT_CONVERGED when the final Jacobi sweeps do
+ *           not converge.
  *  CHOL_* : A (and G) are formed in FP32 and factored in FP64; L and L^-1 are stored in
  *           FP32.  d_status: NOT_PD on a non-positive pivot.
- *  prec   : GIFT_PREC_FP32 forms A (and G) with FP32 SIMT accumulation.  GIFT_PREC_TC with
- *           BF16 activations (d a multiple of 256, T of 64) forms them on the tensor cores:
- *           exact BF16 products, tensor-core FP32 accumulation over T (not round to
- *           nearest); other cases fall back to the FP32 path.
+ *  prec   : GIFT_PREC_FP32 forms A (and G) on the tensor cores from exact three-term BF16
+ *           splits of FP32 activations (BF16 activations are their own single term), each
+ *           64-deep chunk in a fresh FP32 accumulator: FP32 accuracy.  GIFT_PREC_TC with BF16
+ *           activations (d a multiple of 256, T of 64) accumulates over all of T inside the
+ *           tensor cores (their summation order, not round to nearest), and the rank-r
+ *           sketch keeps two terms of its FP32 operands (about 16 mantissa bits).
  *  ws     : device workspace of gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ..., T, ...)
- *           bytes; it includes a BF16 transpose of the activations (max d x T x 2 bytes).
+ *           bytes (term planes of the activations and of Q, the partial sums, the FP64
+ *           Cholesky scratch).
  * Returns INVALID_ARG on null pointers, T < 1, rank outside [1, min(32, d_in)]. */
 gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
                                const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,
                                void *ws, size_t ws_bytes, int *d_status, cudaStream_t stream);
+
+/* The factor refresh from K-FAC factors the caller already holds: gift_factor_update
+ * without its first step, for factors combined before they are factored (the average of A
+ * over the data-parallel replicas, or a running average across refreshes, both of which
+ * gift_kfac_factor's output can feed).  [notes] eq. (4) defines A; the factoring is the same
+ * as gift_factor_update's (core idea step 2 eq. (7), simplification 2 eq. (17)), except that
+ * the rank-r sketch multiplies A explicitly and its last Rayleigh-Ritz step forms Q^T (A Q).
+ *  A  : device, d_in x d_in FP32, row-major, symmetric positive semi-definite; read only.
+ *  G  : device, d_out x d_out FP32 (CHOL_TWO_SIDED only, else NULL); read only.
+ *  ws : gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ..., T = 0, ...) bytes.
+ * Returns INVALID_ARG on a null A (or G for CHOL_TWO_SIDED) and on the cases
+ * gift_factor_update rejects; d_status as for gift_factor_update. */
+gift_status gift_factor_update_from_kfac(gift_ctx *ctx, gift_factor *f, const float *A, const float *G,
+                                         uint64_t seed, gift_precision prec, void *ws, size_t ws_bytes,
+                                         int *d_status, cudaStream_t stream);
 
 /* Bytes of the optional U term planes of a rank-r factor (gift_factor.planes). */
 size_t gift_factor_planes_bytes(int d_in);
@@ -222,11 +249,11 @@ gift_status gift_factor_prepare(gift_ctx *ctx, const gift_factor *f, cudaStream_
  * gift_factor_update, for callers that combine factors before factoring them (for example
  * averaging A over the data-parallel replicas or across refreshes).
  *  a     : device, T x d activations of type a_dt, row-major.
- *  prec  : as in gift_factor_update: GIFT_PREC_TC with BF16 activations (d a multiple of
- *          256, T of 64) on the tensor cores, otherwise FP32 SIMT.
+ *  prec  : as in gift_factor_update; without a workspace (GIFT_PREC_FP32 only) the sums
+ *          run in FP32 SIMT arithmetic.
  *  A_out : device, d x d FP32, row-major; receives the full symmetric matrix.
  *  ws    : device workspace of gift_workspace_bytes(GIFT_OP_KFAC_FACTOR, ..., d_out, d_in = d,
- *          T, ...) bytes (the BF16 transpose of the activations); may be NULL with
+ *          T, ...) bytes (the activations' BF16 transpose or term planes); may be NULL with
  *          GIFT_PREC_FP32.
  * Returns INVALID_ARG on null pointers, d < 1, T < 1, or a workspace too small for TC. */
 gift_status gift_kfac_factor(gift_ctx *ctx, const void *a, gift_dtype a_dt, int T, int d, gift_precision prec,

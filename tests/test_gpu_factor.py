@@ -195,3 +195,73 @@ def test_refresh_iterations_stop_when_ritz_values_settle():
     assert st12 == 0 and st40 == 0
     assert torch.equal(f12.mu, f40.mu) and torch.equal(f12.U, f40.U)
     check_lowrank(f40, a.double().cpu().numpy(), 32, st40)
+
+
+def kfac_on_gpu(a, prec="fp32"):
+    T, d = a.shape
+    A = torch.empty(d, d, device=DEV)
+    n = G.gift_workspace_bytes(ctx(), "kfac_factor", "identity", "e4m3", "tensor", d, d, T)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    G.gift_kfac_factor(ctx(), a, A, prec=prec, ws=w)
+    return A
+
+
+def from_kfac(kind, A, d_out, Gm=None, rank=32, seed=7):
+    d_in = A.shape[0]
+    f = G.Factor.empty(kind, d_out, d_in, rank)
+    n = G.gift_workspace_bytes(ctx(), "factor_update", kind, "e4m3", "tensor", d_out, d_in, 0, rank)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    st = status()
+    G.gift_factor_update_from_kfac(ctx(), f, A, Gm, seed=seed, ws=w, status=st)
+    torch.cuda.synchronize()
+    return f, int(st.item())
+
+
+@pytest.mark.parametrize("d_in", [1024, 64], ids=["tensor-core", "small"])
+def test_from_kfac_replica_average(d_in):
+    # the factor of A averaged over four replicas' K-FAC factors equals the factor of all their
+    # activations together (equal T per replica): eigenpairs checked against the concatenation
+    spec = synth.LayerSpec("m", 128, d_in, T=1024, exponent=1.2, act_dtype=torch.bfloat16)
+    Q = synth.haar_orthogonal(d_in, synth.seed_for(9, 3, stream=1), device="cuda")
+    s = synth.layer_spectrum(spec, 9, 3, device="cuda")
+    acts = [synth.activations(spec.T, d_in, s, Q, synth.seed_for(9, 3, r, stream=2), "cuda", torch.bfloat16)
+            for r in range(4)]
+    A = sum(kfac_on_gpu(a) for a in acts) / 4.0
+    f, st = from_kfac("lowrank", A, 128)
+    a64 = torch.cat(acts).double().cpu().numpy()
+    check_lowrank(f, a64, 32, st)
+
+
+def test_from_kfac_matches_activations_path():
+    # the explicit-sketch refresh from the activations and the refresh from the same A agree
+    # within the eigenvalue tolerance (they differ only in how the last Rayleigh-Ritz step forms
+    # Q^T A Q), with the trace and so sigma taken from the same A
+    spec = synth.LayerSpec("m", 128, 2048, T=2048, exponent=1.0, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 5, 1, 1, device="cuda")
+    f1, _, st1 = run_factor("lowrank", a, 128, sketch=1)
+    f2, st2 = from_kfac("lowrank", kfac_on_gpu(a), 128)
+    assert st1 == 0 and st2 == 0
+    np.testing.assert_allclose(f2.mu.cpu().numpy(), f1.mu.cpu().numpy(), rtol=1e-3)
+    assert abs(float(f2.sigma.item()) - float(f1.sigma.item())) <= 1e-3 * abs(float(f1.sigma.item()))
+    check_lowrank(f2, a.double().cpu().numpy(), 32, st2)
+
+
+@pytest.mark.parametrize("kind", ["chol_input", "chol_two_sided"])
+def test_from_kfac_cholesky_bit_identical(kind):
+    # the Cholesky kinds from A (and G) formed by gift_kfac_factor give the same factors, bit
+    # for bit, as the refresh from the activations (the same K-FAC product, the same FP64 factoring)
+    rng = np.random.default_rng(21)
+    T, d_in, d_out = 1024, 384, 256
+    a = t(rng.standard_normal((T, d_in)))
+    delta = t(rng.standard_normal((T, d_out))) if kind == "chol_two_sided" else None
+    f1, _, st1 = run_factor(kind, a, d_out, delta=delta)
+    A = kfac_on_gpu(a)
+    Gm = kfac_on_gpu(delta) if delta is not None else None
+    f2, st2 = from_kfac(kind, A, d_out, Gm=Gm)
+    assert st1 == 0 and st2 == 0
+    assert torch.equal(f1.LA, f2.LA) and torch.equal(f1.LAinv, f2.LAinv)
+    if kind == "chol_two_sided":
+        assert torch.equal(f1.LG, f2.LG) and torch.equal(f1.LGinv, f2.LGinv)
+    # and L L^T = A for the given A
+    LA = f2.LA.cpu().double().numpy()
+    assert rel_fro(LA @ LA.T, A.cpu().double().numpy()) <= 1e-5
