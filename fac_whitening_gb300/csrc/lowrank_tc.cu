@@ -49,7 +49,9 @@ constexpr long long kWaitBudget = 4000000000LL;
 struct PipeParams {
   LrApply a;
   int tiles_n, tiles_total;
-  int cpr;   // > 0: CTAs per row block (row-aligned schedule); 0: contiguous tile ranges
+  int cpr;    // > 0: CTAs per row block (row-aligned schedule); 0: contiguous tile ranges
+  int unit;   // tiles handed out together: 2 for the 128 x 128 block epilogues (a block's two
+              // 64-column tiles go to one CTA, back to back), else 1
 };
 
 template <int NPL>
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
   __shared__ uint64_t bar_afull, bar_aempty, bar_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ uint32_t red[kReadWarps];
+  __shared__ uint32_t redb[2][kReadWarps];   // block amax, double-buffered across blocks
   __shared__ volatile int failed;
 
   const LrApply &a = P.a;
@@ -80,13 +83,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
   const int d_out = a.d_out, d_in = a.d_in;
   const int b = blockIdx.x;
   int t_begin, t_end;
+  const int un = P.unit;
   if (P.cpr > 0) {
-    const int rb = b / P.cpr, j = b - rb * P.cpr;
-    t_begin = rb * P.tiles_n + (int)(((long long)P.tiles_n * j) / P.cpr);
-    t_end = rb * P.tiles_n + (int)(((long long)P.tiles_n * (j + 1)) / P.cpr);
+    const int rb = b / P.cpr, j = b - rb * P.cpr, units = P.tiles_n / un;
+    t_begin = rb * P.tiles_n + un * (int)(((long long)units * j) / P.cpr);
+    t_end = rb * P.tiles_n + un * (int)(((long long)units * (j + 1)) / P.cpr);
   } else {
-    t_begin = (int)(((long long)P.tiles_total * b) / gridDim.x);
-    t_end = (int)(((long long)P.tiles_total * (b + 1)) / gridDim.x);
+    const int units = P.tiles_total / un;
+    t_begin = un * (int)(((long long)units * b) / gridDim.x);
+    t_end = un * (int)(((long long)units * (b + 1)) / gridDim.x);
   }
 
   if (warp == 0) {
@@ -215,6 +220,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
     const uint32_t *pc_planes = reinterpret_cast<const uint32_t *>(a.split);   // rows of 32 words
     int cur_rb = -1;
     uint32_t ae_par = 0;
+    // 128 x 128 blocks: the first tile's values (and residual row) wait for the second tile
+    float vk[32];
+    uint32_t mk = 0;
+    float *rk = nullptr;
+    int bpar = 0;
+    // FP8 codes of 32 values of a row (and, with error feedback, the residual they leave)
+    auto pack_fp8_row = [&](const float *vv, const ScalePair &p, uint8_t *dst, float *rdst) {
+      uint32_t w4[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float *x = vv + 4 * h;
+        w4[h] = pack4_fp8<F>(__fmul_rn(x[0], p.m), __fmul_rn(x[1], p.m), __fmul_rn(x[2], p.m), __fmul_rn(x[3], p.m));
+      }
+      if (!dst) return;
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+      d4[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      d4[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+      if (rdst) {
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          float e[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            e[k] = __fsub_rn(vv[4 * h + k], __fmul_rn(dec_fp8<F>((w4[h] >> (8 * k)) & 0xFFu), p.s));
+          reinterpret_cast<float4 *>(rdst)[h] = make_float4(e[0], e[1], e[2], e[3]);
+        }
+      }
+    };
     for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
       const int rb = t / P.tiles_n, cb = t - rb * P.tiles_n;
       const int s = i % kStages, acc_i = i & 1;
@@ -280,6 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
         v[4 * c + 3] = fmaf(alpha, w[c].w, __uint_as_float(raw[4 * c + 3]));
       }
       const bool in = row < d_out && (c0 + 32 * half) < d_in;   // d_in is a multiple of 32
+      // error feedback: the tensor quantised is U~ = W~ + R
+      float *rrow = (a.R && in) ? a.R + (size_t)row * d_in + c0 + 32 * half : nullptr;
+      if (rrow) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 r4 = reinterpret_cast<const float4 *>(rrow)[c];
+          v[4 * c + 0] = __fadd_rn(v[4 * c + 0], r4.x);
+          v[4 * c + 1] = __fadd_rn(v[4 * c + 1], r4.y);
+          v[4 * c + 2] = __fadd_rn(v[4 * c + 2], r4.z);
+          v[4 * c + 3] = __fadd_rn(v[4 * c + 3], r4.w);
+        }
+      }
       if (EPI == LR_AMAX && in) {
         // the B planes are stacked in one tensor, so columns past the matrix edge hold
         // neighbouring data: they are kept out of the amax (and never stored)
@@ -302,18 +347,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
                 *reinterpret_cast<const float4 *>(st + (c16 >> 3) * kWBox + sw128(rr, c16 & 7));
         }
       }
-      if (EPI == LR_PACK_TENSOR) {
-        uint32_t w4[8];
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          const float *x = v + 4 * h;
-          w4[h] = pack4_fp8<F>(__fmul_rn(x[0], sp.m), __fmul_rn(x[1], sp.m), __fmul_rn(x[2], sp.m),
-                               __fmul_rn(x[3], sp.m));
-        }
+      if (EPI == LR_PACK_TENSOR)
+        pack_fp8_row(v, sp, in ? a.codes + (size_t)row * d_in + c0 + 32 * half : nullptr, rrow);
+      if (EPI == LR_BLOCK || EPI == LR_BLOCK_AMAX) {
+        // 128 x 128 block scaling (d_in % 128 == 0): the block's amax over both of its tiles,
+        // then both tiles packed with the block's scale
+        uint32_t mb = 0;
         if (in) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (size_t)row * d_in + c0 + 32 * half);
-          dst[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          dst[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mb = max(mb, abs_bits(v[e]));
+        }
+        if ((cb & 1) == 0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) vk[e] = v[e];
+          mk = mb;
+          rk = rrow;
+        } else {
+          mb = warp_max_u32(max(mb, mk));
+          if (lane == 0) redb[bpar][warp] = mb;
+          tc::named_bar_sync(2, 32 * kReadWarps);
+          uint32_t m = 0;
+#pragma unroll
+          for (int w = 0; w < kReadWarps; ++w) m = max(m, redb[bpar][w]);
+          bpar ^= 1;
+          const int blk = rb * (d_in / 128) + (cb >> 1);
+          if (EPI == LR_BLOCK_AMAX) {
+            if (tid == 0) {
+              atomicMax(reinterpret_cast<uint32_t *>(a.amax_ws) + blk, m);
+              if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+            }
+          } else {
+            const float bam = a.amax_in ? a.amax_in[blk] : __uint_as_float(m);
+            const ScalePair bp = scale_pair(bam, fmax_of<F>());
+            if (tid == 0) {
+              if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+              reinterpret_cast<float *>(a.scales)[blk] = bp.s;
+              if (a.amax_out) a.amax_out[blk] = bam;
+            }
+            uint8_t *crow = a.codes + (size_t)row * d_in + c0 + 32 * half;
+            pack_fp8_row(vk, bp, in ? crow - kTileN : nullptr, rk);
+            pack_fp8_row(v, bp, in ? crow : nullptr, rrow);
+          }
         }
       }
       if (EPI == LR_NVFP4) {
@@ -331,6 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_lr_apply_pipe(const __grid_cons
           cw[2 * g] = pack8_e2m1(y);
           cw[2 * g + 1] = pack8_e2m1(y + 8);
           sc |= (uint16_t)grp.e_code << (8 * g);
+          if (rrow) {   // element e of the group sits in word e / 8, bits 4 (e % 8)
+            const float ev = dec_e4m3(grp.e_code);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t word = cw[2 * g + (q >> 1)];
+              float e4[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                e4[k] = __fsub_rn(v[16 * g + 4 * q + k], nvfp4_deq((word >> (16 * (q & 1) + 4 * k)) & 0xFu, ev, s_t));
+              reinterpret_cast<float4 *>(rrow + 16 * g)[q] = make_float4(e4[0], e4[1], e4[2], e4[3]);
+            }
+          }
         }
         if (in) {
           *reinterpret_cast<uint4 *>(a.codes + (((size_t)row * d_in + c0 + 32 * half) >> 1)) =
@@ -719,16 +805,19 @@ size_t lr_pipe_split_floats(int d_out, int d_in) {
 }
 
 // The pipelined apply covers the per-tensor FP8, NVFP4, amax and store epilogues with
-// d_in % 32 == 0 (TMA boxes of 32 columns, 16-byte aligned rows), 16-byte aligned tensors,
-// rank <= 32, no residual and a term-plane workspace; other cases use the FP32-SIMT apply
-// in lowrank.cu.
+// d_in % 32 == 0 (TMA boxes of 32 columns, 16-byte aligned rows) and the 128 x 128 block FP8
+// and block amax epilogues with d_in % 128 == 0, with or without a residual, for 16-byte
+// aligned tensors, rank <= 32 and a term-plane workspace; other cases use the FP32-SIMT
+// apply in lowrank.cu.
 bool lr_apply_tc_ok(const LrApply &a, int epi) {
-  if (epi != LR_AMAX && epi != LR_PACK_TENSOR && epi != LR_NVFP4 && epi != LR_STORE) return false;
+  const bool block = (epi == LR_BLOCK || epi == LR_BLOCK_AMAX);
+  if (epi != LR_AMAX && epi != LR_PACK_TENSOR && epi != LR_NVFP4 && epi != LR_STORE && !block) return false;
   if (!a.split || !a.u_planes) return false;
-  bool ok = (a.d_in % 32 == 0) && aligned16(a.X) && aligned16(a.split) && aligned16(a.u_planes) && !a.R &&
-            (!a.tout || aligned16(a.tout)) && a.rank >= 1 && a.rank <= 32;
+  if (block && a.d_in % 128 != 0) return false;
+  bool ok = (a.d_in % 32 == 0) && aligned16(a.X) && aligned16(a.split) && aligned16(a.u_planes) &&
+            (!a.R || aligned16(a.R)) && (!a.tout || aligned16(a.tout)) && a.rank >= 1 && a.rank <= 32;
   if (epi == LR_STORE) ok = ok && aligned16(a.out);
-  if (epi == LR_PACK_TENSOR || epi == LR_NVFP4) ok = ok && aligned16(a.codes);
+  if (epi == LR_PACK_TENSOR || epi == LR_NVFP4 || epi == LR_BLOCK) ok = ok && aligned16(a.codes);
   if (epi == LR_NVFP4) ok = ok && ((uintptr_t)a.scales & 1) == 0;   // two scale bytes per store
   return ok && tensor_map_encoder() != nullptr;
 }
@@ -756,13 +845,14 @@ static cudaError_t pipe_launch(const Launch &L, const LrApply &a) {
   PipeParams P;
   P.a = a;
   P.tiles_n = (a.d_in + kTileN - 1) / kTileN;
+  P.unit = (EPI == LR_BLOCK || EPI == LR_BLOCK_AMAX) ? 2 : 1;
   const int tiles_m = (a.d_out + kTileM - 1) / kTileM;
   P.tiles_total = P.tiles_n * tiles_m;
   int grid;
   if (tiles_m <= L.sms) {
     // row-aligned: every CTA stays in one row block, so A is loaded once per CTA
     P.cpr = L.sms / tiles_m;
-    if (P.cpr > P.tiles_n) P.cpr = P.tiles_n;
+    if (P.cpr > P.tiles_n / P.unit) P.cpr = P.tiles_n / P.unit;
     grid = tiles_m * P.cpr;
   } else {
     P.cpr = 0;
@@ -789,6 +879,10 @@ static cudaError_t pipe_dispatch(const Launch &L, int epi, int fmt, const LrAppl
     case LR_PACK_TENSOR:
       return fmt == GIFT_FMT_E5M2 ? pipe_launch<LR_PACK_TENSOR, FMT_E5M2, NPL>(L, a)
                                   : pipe_launch<LR_PACK_TENSOR, FMT_E4M3, NPL>(L, a);
+    case LR_BLOCK_AMAX: return pipe_launch<LR_BLOCK_AMAX, FMT_E4M3, NPL>(L, a);
+    case LR_BLOCK:
+      return fmt == GIFT_FMT_E5M2 ? pipe_launch<LR_BLOCK, FMT_E5M2, NPL>(L, a)
+                                  : pipe_launch<LR_BLOCK, FMT_E4M3, NPL>(L, a);
   }
   return cudaErrorInvalidValue;
 }
@@ -809,7 +903,7 @@ static int fused_plan(const Launch &L, const LrApply &a, int *cpr_out) {
 
 bool lr_encode_fused_ok(const Launch &L, const LrApply &a, int epi) {
   if (epi != LR_PACK_TENSOR && epi != LR_NVFP4) return false;
-  if (!lr_apply_tc_ok(a, epi) || !a.grid_counter) return false;
+  if (!lr_apply_tc_ok(a, epi) || !a.grid_counter || a.R) return false;
   int cpr = 0;
   return fused_plan(L, a, &cpr) > 0;
 }

@@ -225,3 +225,66 @@ def test_factor_update_fills_planes():
     G.gift_factor_prepare(ctx(), f)
     torch.cuda.synchronize()
     assert torch.equal(got, f.planes) and int(got.count_nonzero()) > 0
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    # 200 rows: the last 128-row block is clipped; d_in 512 keeps the tensor-core apply
+    return make_layer(200, 512, 1024, 1.0, 3, R=1)
+
+
+@pytest.mark.parametrize("fmt,scaling", [("e4m3", "tensor"), ("nvfp4", "tensor"), ("e5m2", "block128"),
+                                         ("e4m3", "block128")])
+@pytest.mark.parametrize("which", ["c3", "ragged"])
+def test_lowrank_error_feedback_formats(which, fmt, scaling, request):
+    # error feedback through the tensor-core apply (Algorithm 1: U~ = W~ + R, then
+    # R <- U~ - deq(Q(U~))): U~ within the transform tolerance of the oracle's, and the codes,
+    # scales and new residual bit-exact against the oracle's quantiser applied to the GPU's U~
+    Ws, F, _ = request.getfixturevalue(which)
+    W = Ws[0]
+    R0 = (0.3 * np.std(W) * np.random.default_rng(5).standard_normal(W.shape)).astype(np.float32)
+    f = factor_to_gpu("lowrank", *W.shape, F=F)
+    out = encode(f, W, fmt, scaling, residual=R0)
+    assert out["status"] == 0
+    Ut = out["tout"]
+    assert rel_fro(Ut, O.lowrank_whiten(W, F) + R0) <= TOL
+    q = O.quantize(Ut, fmt, scaling)
+    np.testing.assert_array_equal(out["codes"], q["codes"])
+    np.testing.assert_array_equal(out["scales"], q["scales"])
+    np.testing.assert_array_equal(out["residual"], (Ut.astype(np.float64) - O.dequantize_any(q, fmt, scaling))
+                                  .astype(np.float32))
+
+
+@pytest.mark.parametrize("which", ["c3", "ragged", "tiny"])
+def test_lowrank_block_amax_matches_transformed(which, request):
+    # gift_amax with 128 x 128 blocks returns each block's amax of exactly the tensor that
+    # gift_encode quantises
+    Ws, F, _ = request.getfixturevalue(which)
+    W = Ws[-1]
+    d_out, d_in = W.shape
+    f = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    nb = ((d_out + 127) // 128) * ((d_in + 127) // 128)
+    acc = torch.zeros(nb, dtype=torch.float32, device=DEV)
+    G.gift_amax(ctx(), f, t(W), "e4m3", "block128", acc, ws=ws("amax", "lowrank", "e4m3", "block128", d_out, d_in))
+    torch.cuda.synchronize()
+    out = encode(f, W, "e4m3", "block128")
+    got = acc.cpu().numpy()
+    np.testing.assert_array_equal(got, out["amax"])
+    np.testing.assert_array_equal(got.reshape(out["scales"].shape), O.block_amax(out["tout"]))
+
+
+def test_lowrank_block_unaligned_simt():
+    # d_in not a multiple of 128: the FP32-SIMT apply, same contract
+    rng = np.random.default_rng(6)
+    a = rng.standard_normal((600, 288)) * np.linspace(3, 0.2, 288)
+    F = O.lowrank_factor_from_A(O.kfac_factor(a), r=32)
+    F = O.LowRankFactor(F.U.astype(np.float32), F.mu.astype(np.float32), np.float32(F.sigma))
+    W = rng.standard_normal((200, 288)).astype(np.float32)
+    R0 = (0.1 * rng.standard_normal(W.shape)).astype(np.float32)
+    f = factor_to_gpu("lowrank", 200, 288, F=F)
+    out = encode(f, W, "e4m3", "block128", residual=R0)
+    assert rel_fro(out["tout"], O.lowrank_whiten(W, F) + R0) <= TOL
+    q = O.quantize(out["tout"], "e4m3", "block128")
+    np.testing.assert_array_equal(out["codes"], q["codes"])
+    np.testing.assert_array_equal(out["residual"], (out["tout"].astype(np.float64) - O.dequantize_any(q, "e4m3", "block128"))
+                                  .astype(np.float32))
