@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -159,13 +160,20 @@ __global__ void __launch_bounds__(256) k_split_planes(const Src *__restrict__ sr
   if (nt > 2) *reinterpret_cast<uint4 *>(planes + 2 * plane + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
 }
 
-template <int BN>
+// SB > 1 (A a single term): the products x y_0 .. x y_{SB-1} are one MMA per K step with the
+// B term tiles stacked as N = SB x BN rows (they sit back to back in the stage), so A is read
+// from shared memory once per K step instead of once per product; each product lands in its
+// own BN-column group of the accumulator and the epilogue adds the groups, smallest first.
+template <int BN, int SB>
 __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_constant__ GemmTcParams P,
                                                              const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB, int *status) {
   extern __shared__ uint8_t dsm[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023);
-  constexpr int NACC = 4;                       // TMEM accumulators (a fresh one per chunk)
+  constexpr int NACC = (SB > 1) ? 2 : 4;       // TMEM accumulators (a fresh one per chunk)
+  constexpr int ACOLS = SB * BN;                // columns of one accumulator
+  constexpr uint32_t TCOLS = (NACC * ACOLS <= 256) ? 256u : 512u;
+  static_assert(NACC * ACOLS <= 512 && ACOLS <= 256, "accumulators exceed tensor memory or the MMA's N");
   __shared__ uint64_t full[kGMaxStages], empty[kGMaxStages], afull[NACC], aempty[NACC];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int failed;
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
   if (P.skip && *P.skip) return;
 
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base_sh, NACC * BN);
+    tc::tmem_alloc(&tmem_base_sh, TCOLS);
     tc::tmem_relinquish();
   }
   if (tid == 32) {
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
   } else if (warp == kGEpiWarps + 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16(kGM, BN);
+      constexpr uint32_t idesc = tc::idesc_bf16(kGM, ACOLS);
       // the products' operand offsets, in registers (a dynamically indexed parameter array
       // would be copied to local memory)
       uint32_t offa[kGMaxProducts], offb[kGMaxProducts];
@@ -265,10 +273,17 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
           if (!(ok = wait(&full[s], (uint32_t)phase))) break;
           tc::fence_after_sync();
           const uint32_t base = tc::smem_u32(sm + (size_t)s * P.stage_bytes);
-          const uint32_t d = tmem + (uint32_t)(a * BN);
+          const uint32_t d = tmem + (uint32_t)(a * ACOLS);
+          if (SB > 1) {   // A term 0 against the stacked B terms 0 .. SB-1
+            const uint32_t bb = base + (uint32_t)(P.nta * kGTile);
+#pragma unroll
+            for (int k = 0; k < kGK / 16; ++k)
+              tc::mma_bf16(d, tc::sdesc_kmajor_sw128(base + 32 * k), tc::sdesc_kmajor_sw128(bb + 32 * k), idesc,
+                           k > 0 ? 1u : 0u);
+          }
 #pragma unroll
           for (int q = 0; q < kGMaxProducts; ++q) {
-            if (q < P.nprod) {
+            if (SB == 1 && q < P.nprod) {
               const uint32_t ab = base + offa[q], bb = base + offb[q];
 #pragma unroll
               for (int k = 0; k < kGK / 16; ++k)
@@ -305,8 +320,39 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
       bool ok = true;
       // with N = 64, two chunks per round trip: both accumulators are read with one completion
       // wait, then added in chunk order (with N = 128 the registers hold one chunk)
-      constexpr int CG = (BN == 64) ? 2 : 1;
-      for (int c = c0; c < c1; c += CG) {
+      constexpr int CG = (BN == 64 && SB == 1) ? 2 : 1;
+      if (SB > 1) {
+        for (int c = c0; c < c1; ++c) {
+          if (!(ok = wait(&afull[a], (uint32_t)aphase))) break;
+          tc::fence_after_sync();
+          uint32_t r[SB][NC];
+#pragma unroll
+          for (int gq = 0; gq < SB; ++gq)
+#pragma unroll
+            for (int g = 0; g < NC / 32; ++g)
+              tc::tmem_ld32_nowait(tmem + lane_off + (uint32_t)(a * ACOLS + gq * BN + NC * half + 32 * g),
+                                   r[gq] + 32 * g);
+#pragma unroll
+          for (int gq = 0; gq < SB; ++gq)
+#pragma unroll
+            for (int g = 0; g < NC / 32; ++g) tc::tmem_wait_ld(r[gq] + 32 * g);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&aempty[a]);
+          if (++a == NACC) {
+            a = 0;
+            aphase ^= 1;
+          }
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            float sum = __uint_as_float(r[SB - 1][i]);
+#pragma unroll
+            for (int gq = SB - 2; gq >= 0; --gq) sum = __fadd_rn(sum, __uint_as_float(r[gq][i]));
+            acc[i] = __fadd_rn(acc[i], sum);
+          }
+        }
+      }
+      for (int c = c0; c < c1 && SB == 1; c += CG) {
         const int n2 = (c1 - c) < CG ? (c1 - c) : CG;
         const int a1 = (a + 1 == NACC) ? 0 : a + 1;
         const int aphase1 = (a + 1 == NACC) ? (aphase ^ 1) : aphase;
@@ -314,8 +360,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
         if (n2 == 2 && !(ok = wait(&afull[a1], (uint32_t)aphase1))) break;
         tc::fence_after_sync();
         uint32_t r[CG][NC];
-        const uint32_t col = tmem + lane_off + (uint32_t)(a * BN + NC * half);
-        const uint32_t col1 = tmem + lane_off + (uint32_t)(a1 * BN + NC * half);
+        const uint32_t col = tmem + lane_off + (uint32_t)(a * ACOLS + NC * half);
+        const uint32_t col1 = tmem + lane_off + (uint32_t)(a1 * ACOLS + NC * half);
 #pragma unroll
         for (int g = 0; g < NC / 32; ++g) tc::tmem_ld32_nowait(col + 32 * g, r[0] + 32 * g);
         if (CG == 2 && n2 == 2) {
@@ -370,7 +416,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_split(const __grid_consta
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, NACC * BN);
+    tc::tmem_dealloc(tmem, TCOLS);
   }
 }
 
@@ -521,15 +567,25 @@ cudaError_t launch_gemm_planes(const Launch &L, const GemmPlanes &g) {
   P.ldc = ldc;
   const int smem = P.stages * P.stage_bytes + 1024;
   const int grid = P.ntiles < L.sms ? P.ntiles : L.sms;
+  // a single A term: its products with B terms 0 .. nprod-1 as one stacked MMA per K step
+  // (the products are (0, j), j < nprod, whenever nta == 1)
+  const int sb = (g.nta == 1 && P.nprod > 1 && P.nprod * BN <= 256) ? P.nprod : 1;
   cudaError_t e;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e2 = ensure_dynamic_smem<decltype(kern)::value>(smem);
+    if (e2 != cudaSuccess) return e2;
+    decltype(kern)::value<<<grid, kGThreads, smem, L.stream>>>(P, tmA, tmB, L.status);
+    return cudaGetLastError();
+  };
   if (BN == 64) {
-    if ((e = ensure_dynamic_smem<k_gemm_split<64>>(smem)) != cudaSuccess) return e;
-    k_gemm_split<64><<<grid, kGThreads, smem, L.stream>>>(P, tmA, tmB, L.status);
+    if (sb == 3) e = go(std::integral_constant<decltype(&k_gemm_split<64, 3>), &k_gemm_split<64, 3>>{});
+    else if (sb == 2) e = go(std::integral_constant<decltype(&k_gemm_split<64, 2>), &k_gemm_split<64, 2>>{});
+    else e = go(std::integral_constant<decltype(&k_gemm_split<64, 1>), &k_gemm_split<64, 1>>{});
   } else {
-    if ((e = ensure_dynamic_smem<k_gemm_split<128>>(smem)) != cudaSuccess) return e;
-    k_gemm_split<128><<<grid, kGThreads, smem, L.stream>>>(P, tmA, tmB, L.status);
+    if (sb == 2) e = go(std::integral_constant<decltype(&k_gemm_split<128, 2>), &k_gemm_split<128, 2>>{});
+    else e = go(std::integral_constant<decltype(&k_gemm_split<128, 1>), &k_gemm_split<128, 1>>{});
   }
-  if ((e = cudaGetLastError()) != cudaSuccess || g.ksplit == 1) return e;
+  if (e != cudaSuccess || g.ksplit == 1) return e;
   const size_t n = (size_t)g.M * g.N;
   int sg = (int)((n + 255) / 256);
   if (sg > L.sms * 4) sg = L.sms * 4;
