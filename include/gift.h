@@ -199,9 +199,9 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
  *           forms Y = A Q (by default as a^T (a Q) / T, A never formed; GIFT_OPT_SKETCH
  *           selects the explicit product) and re-orthonormalises Q by CholQR2 with
  *           compensated FP32 Gram sums; Rayleigh-Ritz steps (FP32 parallel Jacobi) rotate
- *           Q on the first two steps and every fourth, and stop the iteration once the top
- *           `rank` Ritz values move by less than a quarter ulp (at most
- *           GIFT_OPT_SUBSPACE_ITERS steps, default 16).  The last Rayleigh-Ritz step takes
+ *           Q on the first two steps and every fourth, and stop the iteration once each of
+ *           the top `rank` Ritz pairs has a residual ||A u - theta u|| <= 1e-4 theta (at
+ *           most GIFT_OPT_SUBSPACE_ITERS steps, default 16).  The last Rayleigh-Ritz step takes
  *           Q^T A Q as the Gram matrix of a Q.  For d_in <= 64 the Gram, Cholesky and
  *           eigensolve run in FP64 on A itself.  U = Q V[:, :rank]; sigma =
  *           (tr A - sum mu) / (d_in - rank) (sigma = 1 when rank == d_in).  d_status:
