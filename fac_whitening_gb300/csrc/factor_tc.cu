@@ -96,31 +96,47 @@ __device__ __forceinline__ void two_sum_add(float &s, float &c, float x) {
   s = t;
 }
 
-// out = sum over the CTAs' partials in CTA order (compensated), symmetrised when sym; one
-// thread per entry.
+// out = the sum of the CTAs' partials (compensated), symmetrised when sym.  Eight threads per
+// entry: thread u sums partials u, u + 8, u + 16, ... in order, then thread 0 of the group adds
+// the eight sums in thread order, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(256) k_gram_sum(const float *__restrict__ parts, int nparts, int k, bool sym,
                                                   float scale, float *__restrict__ out, const int *skip) {
   if (skip && *skip) return;
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= k * k) return;
-  const int i = idx / k, j = idx % k;
+  const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int idx = gid >> 3, sub = gid & 7, lane = threadIdx.x & 31;
+  const bool valid = idx < k * k;
+  const int i = valid ? idx / k : 0, j = valid ? idx % k : 0;
+  const size_t kk = (size_t)k * k;
   float s = 0.0f, c = 0.0f;
-  for (int p0 = 0; p0 < nparts; p0 += 8) {
-    float x[8], y[8];
+  if (valid) {
+    for (int p0 = sub; p0 < nparts; p0 += 64) {
+      float x[8], y[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {   // the loads first, then the dependent sums
-      const int p = p0 + u;
-      x[u] = p < nparts ? parts[(size_t)p * k * k + idx] : 0.0f;
-      y[u] = (sym && p < nparts) ? parts[(size_t)p * k * k + (size_t)j * k + i] : 0.0f;
-    }
+      for (int u = 0; u < 8; ++u) {   // the loads first, then the dependent sums
+        const int p = p0 + 8 * u;
+        x[u] = p < nparts ? parts[(size_t)p * kk + idx] : 0.0f;
+        y[u] = (sym && p < nparts) ? parts[(size_t)p * kk + (size_t)j * k + i] : 0.0f;
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      two_sum_add(s, c, x[u]);
-      two_sum_add(s, c, y[u]);
+      for (int u = 0; u < 8; ++u) {
+        two_sum_add(s, c, x[u]);
+        two_sum_add(s, c, y[u]);
+      }
     }
   }
-  const float v = __fadd_rn(s, c);
-  out[idx] = __fmul_rn(sym ? 0.5f * v : v, scale);
+#pragma unroll
+  for (int u = 1; u < 8; ++u) {
+    const float su = __shfl_sync(0xFFFFFFFFu, s, (lane & ~7) + u);
+    const float cu = __shfl_sync(0xFFFFFFFFu, c, (lane & ~7) + u);
+    if (sub == 0) {
+      two_sum_add(s, c, su);
+      c = __fadd_rn(c, cu);
+    }
+  }
+  if (valid && sub == 0) {
+    const float v = __fadd_rn(s, c);
+    out[idx] = __fmul_rn(sym ? 0.5f * v : v, scale);
+  }
 }
 
 // =====================================================================================
@@ -480,7 +496,7 @@ cudaError_t launch_gram_tall(const Launch &L, const float *X, const float *Y, in
   k_gram_tall<<<ctas, 256, 0, L.stream>>>(X, Y, d, k, rows, parts, skip);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_gram_sum<<<(k * k + 255) / 256, 256, 0, L.stream>>>(parts, ctas, k, sym, scale, out, skip);
+  k_gram_sum<<<(8 * k * k + 255) / 256, 256, 0, L.stream>>>(parts, ctas, k, sym, scale, out, skip);
   return cudaGetLastError();
 }
 
