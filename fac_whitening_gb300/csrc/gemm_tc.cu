@@ -437,9 +437,11 @@ PFN_cuTensorMapEncodeTiled_v12000 gemm_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // Blocked BF16 planes viewed as rows of 64 elements (128 bytes): boxes of 64 x box_rows,
-// 128-byte swizzle.
-bool plane_map(CUtensorMap *m, const uint16_t *base, uint64_t rows_total, uint32_t box_rows = 128) {
+// 128-byte swizzle.  (Also used by the FP64-accurate GEMM.)
+bool plane_map(CUtensorMap *m, const uint16_t *base, uint64_t rows_total, uint32_t box_rows) {
   auto enc = gemm_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kGK, rows_total};
@@ -450,6 +452,8 @@ bool plane_map(CUtensorMap *m, const uint16_t *base, uint64_t rows_total, uint32
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 int pad_to(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -514,7 +518,7 @@ cudaError_t launch_gemm_planes(const Launch &L, const GemmPlanes &g) {
   const int BN = (g.N <= 64 && !g.lower_tiles) ? 64 : 128;   // the tile's columns
   CUtensorMap tmA, tmB;
   const uint64_t nchl = (uint64_t)(ldk / kGK);
-  if (!plane_map(&tmA, g.pa, (uint64_t)g.nta * rows_a * nchl) ||
+  if (!plane_map(&tmA, g.pa, (uint64_t)g.nta * rows_a * nchl, 128) ||
       !plane_map(&tmB, g.pb, (uint64_t)g.ntb * rows_b * nchl, (uint32_t)BN))
     return cudaErrorInvalidValue;
   GemmTcParams P;

@@ -290,9 +290,15 @@ cudaError_t launch_sum_slices(const Launch &L, const double *parts, int splits, 
 cudaError_t launch_mirror_lower(const Launch &L, float *A, int n);
 cudaError_t launch_f32_to_f64(const Launch &L, const float *x, double *y, size_t n);
 cudaError_t launch_f64_to_f32(const Launch &L, const double *x, float *y, size_t n, bool zero_upper, int n_cols);
-// Cholesky A = L L^T and L^-1 in FP64 (A is overwritten by L, Linv receives L^-1), n x n.
+// Cholesky A = L L^T and L^-1 in FP64 (A is overwritten by L, Linv receives L^-1), n x n;
+// the large products of the recursion on the tensor cores (ozaki_tc.cu).
 cudaError_t launch_chol_inv(const Launch &L, double *A, double *Linv, int n, double *work);
 size_t chol_inv_work_doubles(int n);
+// ---- ozaki_tc.cu: FP64-accurate GEMM from exact BF16 slices on the tensor cores ----------
+size_t gemm_oz_ws_bytes(int M, int N, int K);
+bool gemm_oz_ok(int M, int N, int K);
+cudaError_t launch_gemm_oz(const Launch &L, const double *A, int lda, bool transA, const double *B, int ldb,
+                           bool transB, double *C, int ldc, int M, int N, int K, double alpha, double beta, void *ws);
 
 // ---- factor.cu --------------------------------------------------------------------------
 cudaError_t launch_philox_gaussian(const Launch &L, float *out, size_t n, uint64_t seed);

@@ -381,52 +381,58 @@ constexpr int kCholBase = 64;
 
 // One CTA: factor the n x n (n <= 64) block at A (leading dimension lda) in place into L
 // (upper part zeroed) and write L^-1 (lower, upper zeroed) at Li (leading dimension ldl).
+// Right-looking: step j takes the pivot, scales column j of L and row j of X (X = I becomes
+// L^-1 by forward elimination alongside), then updates every row below j: S_ic for
+// j < c <= i and X_ic for c <= j, spread over all threads.  One
+// reciprocal square root per step; the rest are multiplications and fused multiply-adds.
 __global__ void __launch_bounds__(256) k_chol_inv_small(double *A, int lda, double *Li, int ldl, int n, int *status) {
   extern __shared__ double chol_sm[];   // two (kCholBase x kCholBase+1) tiles, opt-in size
   double(*S)[kCholBase + 1] = reinterpret_cast<double(*)[kCholBase + 1]>(chol_sm);
   double(*X)[kCholBase + 1] = reinterpret_cast<double(*)[kCholBase + 1]>(chol_sm + kCholBase * (kCholBase + 1));
   __shared__ int bad;
+  __shared__ double rp_sh;
   const int tid = threadIdx.x;
   if (tid == 0) bad = 0;
   for (int idx = tid; idx < n * n; idx += 256) {
     const int i = idx / n, j = idx - i * n;
     S[i][j] = A[(size_t)i * lda + j];
+    X[i][j] = (i == j) ? 1.0 : 0.0;
   }
   __syncthreads();
   for (int j = 0; j < n; ++j) {
     if (tid == 0) {
+      // 1/sqrt(d) from the FP32 estimate and two Newton steps in FP64 (24 -> 48 -> 96 bits),
+      // cheaper on this GPU than its FP64 square root and division
       const double d = S[j][j];
+      double piv = 1.0, r = 1.0;
       if (!(d > 0.0)) {
         bad = 1;
-        S[j][j] = 1.0;
       } else {
-        S[j][j] = sqrt(d);
+        r = (double)rsqrtf((float)d);
+        if (!(r > 0.0) || isinf(r)) r = 1.0 / sqrt(d);   // d beyond FP32 range
+        const double hd = 0.5 * d;
+        r = r * fma(-hd, r * r, 1.5);
+        r = r * fma(-hd, r * r, 1.5);
+        piv = d * r;
       }
+      S[j][j] = piv;
+      rp_sh = r;
     }
     __syncthreads();
-    const double piv = S[j][j];
-    for (int i = j + 1 + tid; i < n; i += 256) S[i][j] = S[i][j] / piv;
+    const double rp = rp_sh;
+    if (tid > j && tid < n) S[tid][j] *= rp;            // column j of L
+    if (tid < 64 && tid <= j) X[j][tid] *= rp;         // row j of L^-1
     __syncthreads();
-    const int m = n - j - 1;
-    for (int idx = tid; idx < m * m; idx += 256) {
-      const int i = j + 1 + idx / m, k = j + 1 + idx % m;
-      if (k <= i) S[i][k] = fma(-S[i][j], S[k][j], S[i][k]);
+    const int rows = n - j - 1;
+    for (int idx = tid; idx < rows * n; idx += 256) {
+      const int i = j + 1 + idx / n, c = idx - (idx / n) * n;
+      if (c > i) continue;
+      const double lij = S[i][j];
+      if (c > j) S[i][c] = fma(-lij, S[c][j], S[i][c]);
+      else X[i][c] = fma(-lij, X[j][c], X[i][c]);
     }
     __syncthreads();
   }
-  // L^-1 by forward substitution, one column per thread
-  for (int c = tid; c < n; c += 256) {
-    for (int i = 0; i < n; ++i) {
-      if (i < c) {
-        X[i][c] = 0.0;
-        continue;
-      }
-      double s = (i == c) ? 1.0 : 0.0;
-      for (int k = c; k < i; ++k) s = fma(-S[i][k], X[k][c], s);
-      X[i][c] = s / S[i][i];
-    }
-  }
-  __syncthreads();
   for (int idx = tid; idx < n * n; idx += 256) {
     const int i = idx / n, j = idx - i * n;
     A[(size_t)i * lda + j] = (j <= i) ? S[i][j] : 0.0;
@@ -441,7 +447,7 @@ __global__ void k_copy_block(const double *src, int lds, double *dst, int ldd, i
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const size_t r = i / cols, c = i - r * cols;
-    dst[r * ldd + c] = (scale == 0.0) ? 0.0 : scale * src[r * lds + c];
+    dst[r * ldd + c] = (scale == 0.0) ? 0.0 : (scale == 1.0) ? src[r * lds + c] : scale * src[r * lds + c];
   }
 }
 
@@ -461,9 +467,19 @@ static cudaError_t dgemm_dd(const Launch &L, const double *A, int lda, bool tA, 
   return launch_dgemm(L, g);
 }
 
+// The recursion's products: on the tensor cores with FP64 accuracy (exact BF16 slices) when a
+// workspace is given and the product is large, else the FP64 SIMT GEMM.
+static cudaError_t gemm_f64(const Launch &L, const double *A, int lda, bool tA, const double *B, int ldb, bool tB,
+                            double *C, int ldc, int M, int N, int K, double alpha, double beta, void *oz) {
+  if (oz && M >= 64 && N >= 64 && K >= 64 && gemm_oz_ok(M, N, K))
+    return launch_gemm_oz(L, A, lda, tA, B, ldb, tB, C, ldc, M, N, K, alpha, beta, oz);
+  return dgemm_dd(L, A, lda, tA, B, ldb, tB, C, ldc, M, N, K, alpha, beta);
+}
+
 // Recursive step on the n x n diagonal block at offset `o` of the full matrices (leading
 // dimension ld).
-static cudaError_t chol_inv_rec(const Launch &L, double *A, double *Li, int ld, int o, int n, double *work) {
+static cudaError_t chol_inv_rec(const Launch &L, double *A, double *Li, int ld, int o, int n, double *work,
+                                void *oz) {
   double *Ab = A + (size_t)o * ld + o;
   double *Lb = Li + (size_t)o * ld + o;
   if (n <= kCholBase) {
@@ -477,30 +493,45 @@ static cudaError_t chol_inv_rec(const Launch &L, double *A, double *Li, int ld, 
   if (n1 >= n) n1 = n - kCholBase;
   const int n2 = n - n1;
   cudaError_t e;
-  if ((e = chol_inv_rec(L, A, Li, ld, o, n1, work)) != cudaSuccess) return e;
+  if ((e = chol_inv_rec(L, A, Li, ld, o, n1, work, oz)) != cudaSuccess) return e;
   double *A21 = Ab + (size_t)n1 * ld;          // n2 x n1
   double *A22 = A21 + n1;                      // n2 x n2
   double *L11i = Lb;                           // n1 x n1
   // L21 = A21 L11^-T  (into work, then back into A21)
-  if ((e = dgemm_dd(L, A21, ld, false, L11i, ld, true, work, n1, n2, n1, n1, 1.0, 0.0)) != cudaSuccess) return e;
+  if ((e = gemm_f64(L, A21, ld, false, L11i, ld, true, work, n1, n2, n1, n1, 1.0, 0.0, oz)) != cudaSuccess) return e;
   if ((e = copy_block(L, work, n1, A21, ld, n2, n1, 1.0)) != cudaSuccess) return e;
   // S = A22 - L21 L21^T
-  if ((e = dgemm_dd(L, A21, ld, false, A21, ld, true, A22, ld, n2, n2, n1, -1.0, 1.0)) != cudaSuccess) return e;
-  if ((e = chol_inv_rec(L, A, Li, ld, o + n1, n2, work)) != cudaSuccess) return e;
+  if ((e = gemm_f64(L, A21, ld, false, A21, ld, true, A22, ld, n2, n2, n1, -1.0, 1.0, oz)) != cudaSuccess) return e;
+  if ((e = chol_inv_rec(L, A, Li, ld, o + n1, n2, work, oz)) != cudaSuccess) return e;
   // (L^-1)21 = -L22^-1 (L21 L11^-1)
   double *L22i = Lb + (size_t)n1 * ld + n1;
   double *Li21 = Lb + (size_t)n1 * ld;
-  if ((e = dgemm_dd(L, A21, ld, false, L11i, ld, false, work, n1, n2, n1, n1, 1.0, 0.0)) != cudaSuccess) return e;
-  if ((e = dgemm_dd(L, L22i, ld, false, work, n1, false, Li21, ld, n2, n1, n2, -1.0, 0.0)) != cudaSuccess) return e;
+  if ((e = gemm_f64(L, A21, ld, false, L11i, ld, false, work, n1, n2, n1, n1, 1.0, 0.0, oz)) != cudaSuccess) return e;
+  if ((e = gemm_f64(L, L22i, ld, false, work, n1, false, Li21, ld, n2, n1, n2, -1.0, 0.0, oz)) != cudaSuccess)
+    return e;
   // upper blocks are zero
   if ((e = copy_block(L, nullptr, 0, Ab + n1, ld, n1, n2, 0.0)) != cudaSuccess) return e;
   return copy_block(L, nullptr, 0, Lb + n1, ld, n1, n2, 0.0);
 }
 
-size_t chol_inv_work_doubles(int n) { return (size_t)n * n / 2 + (size_t)kCholBase * n + 64; }
+// The FP64 scratch of the recursion, then (256-byte aligned) the tensor-core products' slices:
+// every product of the recursion has M, N, K <= n / 2 + 64.
+static size_t chol_base_doubles(int n) { return (size_t)n * n / 2 + (size_t)kCholBase * n + 64; }
+static size_t chol_oz_doubles(int n) {
+  if (n <= kCholBase) return 0;
+  const int h = n / 2 + 128;
+  return gemm_oz_ws_bytes(h, h, h) / 8 + 64;
+}
+
+size_t chol_inv_work_doubles(int n) { return chol_base_doubles(n) + chol_oz_doubles(n); }
 
 cudaError_t launch_chol_inv(const Launch &L, double *A, double *Linv, int n, double *work) {
-  return chol_inv_rec(L, A, Linv, n, 0, n, work);
+  void *oz = nullptr;
+  if (chol_oz_doubles(n) > 0) {
+    uintptr_t p = reinterpret_cast<uintptr_t>(work + chol_base_doubles(n));
+    oz = reinterpret_cast<void *>((p + 255) & ~(uintptr_t)255);
+  }
+  return chol_inv_rec(L, A, Linv, n, 0, n, work, oz);
 }
 
 }  // namespace gift
