@@ -545,13 +545,13 @@ static gift_status factor_update_impl(gift_ctx *ctx, gift_factor *f, const void 
       CK(launch_split_planes(L, A, d_in, d_in, d_in, false, nt, w.apl));
     }
     CK(cudaMemsetAsync(w.flag, 0, sizeof(int), stream));
-    auto orth = [&](float *Y, const int *sk) -> cudaError_t {   // Q = Y R^-1, twice (CholQR2)
+    auto orth = [&](float *Y, const int *sk) -> cudaError_t {   // Q = Y L^-T with Y^T Y = L L^T, twice (CholQR2)
       cudaError_t e = cudaSuccess;
       const float *src = Y;
       for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
         if ((e = launch_gram_tall(L, src, src, d_in, k, w.gparts, w.G32, true, sk)) != cudaSuccess) break;
-        if ((e = launch_chol_rinv32(L, w.G32, k, w.R32, sk)) != cudaSuccess) break;
-        e = launch_right_mul64(L, src, d_in, w.R32, w.Q, sk);
+        if ((e = launch_chol32(L, w.G32, k, w.R32, sk)) != cudaSuccess) break;
+        e = launch_right_trsm64(L, src, d_in, w.R32, w.Q, sk);
         src = w.Q;
       }
       return e;

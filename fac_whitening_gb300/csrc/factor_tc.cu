@@ -140,148 +140,155 @@ __global__ void __launch_bounds__(256) k_gram_sum(const float *__restrict__ part
 }
 
 // =====================================================================================
-// Cholesky G = L L^T of a k x k Gram matrix (k <= 64) and R^-1 = (L^-1)^T (so that
-// Q = Y R^-1 has Q^T Q = I), FP32, one CTA.  A pivot below 1e-10 of the largest diagonal
-// (a numerically rank-deficient block) is replaced by 1.
+// Cholesky G = L L^T of a k x k Gram matrix (k = 64), FP32, one CTA of 256 threads; L is
+// written lower-triangular (upper part zero).  A pivot below 1e-10 of the largest diagonal (a
+// numerically rank-deficient block) is replaced by 1.
+// Blocked by panels of 16 columns: warp 0 factors a panel on its own (16 right-looking steps
+// with warp barriers, two rows per lane), then all threads apply the panel's rank-16 update to
+// the rows and columns after it; two CTA barriers per panel instead of two per column.
 // =====================================================================================
-__global__ void __launch_bounds__(256) k_chol_rinv32(const float *__restrict__ G, float *__restrict__ Rinv,
-                                                     const int *skip) {
+__global__ void __launch_bounds__(256) k_chol32(const float *__restrict__ G, float *__restrict__ Lout,
+                                                const int *skip) {
   if (skip && *skip) return;
-  __shared__ float S[kK][kK + 1], X[kK][kK + 1];
+  __shared__ float S[kK][kK + 1];
   __shared__ float tiny_sh;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;   // 16 x 16 threads, 4 x 4 entries each
-  for (int idx = tid; idx < kK * kK; idx += 256) {
-    const int i = idx >> 6, j = idx & 63;
-    S[i][j] = G[idx];
-    X[i][j] = (i == j) ? 1.0f : 0.0f;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float scale = 0.0f;
-    for (int i = 0; i < kK; ++i) scale = fmaxf(scale, S[i][i]);
-    tiny_sh = scale * 1e-10f + 1e-30f;
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int idx = tid; idx < kK * kK; idx += 256) S[idx >> 6][idx & 63] = G[idx];
+  if (tid < 32) {   // the largest diagonal entry sets the rank-deficiency floor
+    float m = fmaxf(G[tid * kK + tid], G[(tid + 32) * kK + tid + 32]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (tid == 0) tiny_sh = m * 1e-10f + 1e-30f;
   }
   __syncthreads();
   const float tiny = tiny_sh;
-  // step j: the pivot and column j of L (right-looking Cholesky) and row j of X = L^-1 (forward
-  // elimination on the rows of I); then the trailing update of S and the elimination of
-  // column j from the rows of X below
-  for (int j = 0; j < kK; ++j) {
-    const float dj = S[j][j];
-    const float piv = (dj > tiny) ? sqrtf(dj) : 1.0f;
-    const float rp = 1.0f / piv;
-    __syncthreads();   // every thread has read the pivot
-    if (tid < kK) {
-      if (tid > j) S[tid][j] = S[tid][j] * rp;
-      if (tid <= j) X[j][tid] = X[j][tid] * rp;
-      if (tid == j) S[j][j] = piv;
+  for (int p = 0; p < kK / 16; ++p) {
+    const int c0 = 16 * p, c1 = c0 + 16;
+    if (tid < 32) {
+      for (int j = c0; j < c1; ++j) {
+        const float d = S[j][j];
+        const float piv = (d > tiny) ? sqrtf(d) : 1.0f;
+        const float rp = 1.0f / piv;
+        __syncwarp();   // every lane has read the pivot
+        const int r0 = lane, r1 = lane + 32;
+        if (r0 > j) S[r0][j] *= rp;
+        if (r1 > j) S[r1][j] *= rp;
+        if (lane == 0) S[j][j] = piv;
+        __syncwarp();
+        // the panel's columns right of j
+        for (int c = j + 1; c < c1; ++c) {
+          const float lc = S[c][j];
+          if (r0 >= c) S[r0][c] = fmaf(-S[r0][j], lc, S[r0][c]);
+          if (r1 >= c) S[r1][c] = fmaf(-S[r1][j], lc, S[r1][c]);
+        }
+        __syncwarp();
+      }
     }
     __syncthreads();
+    // trailing update: S[r][c] -= sum over the panel of L[r][k] L[c][k], c1 <= c <= r
+    const int m = kK - c1;
+    for (int idx = tid; idx < m * m; idx += 256) {
+      const int r = c1 + idx / m, c = c1 + idx % m;
+      if (c > r) continue;
+      float acc = S[r][c];
 #pragma unroll
-    for (int hi = 0; hi < 4; ++hi)
-#pragma unroll
-      for (int hc = 0; hc < 4; ++hc) {
-        const int i = ty + 16 * hi, c = tx + 16 * hc;
-        if (i > j) {
-          const float lij = S[i][j];
-          if (c > j && c <= i) S[i][c] = fmaf(-lij, S[c][j], S[i][c]);
-          if (c <= j) X[i][c] = fmaf(-lij, X[j][c], X[i][c]);
-        }
-      }
+      for (int k = 0; k < 16; ++k) acc = fmaf(-S[r][c0 + k], S[c][c0 + k], acc);
+      S[r][c] = acc;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   for (int idx = tid; idx < kK * kK; idx += 256) {
-    const int i = idx >> 6, j = idx & 63;
-    Rinv[idx] = X[j][i];
+    const int r = idx >> 6, c = idx & 63;
+    Lout[idx] = (c <= r) ? S[r][c] : 0.0f;
   }
 }
 
 // =====================================================================================
-// Symmetric eigensolver, k <= 64, FP32, one CTA: parallel-order cyclic Jacobi (each round
-// applies k/2 disjoint rotations; every pair once per sweep), the rotation with the smaller
-// angle that zeroes A[p][q] (Golub & Van Loan, "Matrix Computations", sec. 8.5).  A pair is
-// rotated while |A[p][q]| > 1e-6 sqrt(|A[p][p] A[q][q]|) (the relative criterion, which keeps
-// the small eigenvalues of a positive definite matrix to high relative accuracy) and above
-// 2^-21 max(|A[p][p]|, |A[q][q]|) (the FP32 rounding floor of the larger one, below which a
-// rotation only moves noise); the solver stops after a sweep that rotates nothing, or after
-// max_sweeps (then NOT_CONVERGED, when a status word is given).  Eigenvalues descending; V's
-// column c is the eigenvector of evals[c].
+// Symmetric eigensolver, k = 64, FP32, one CTA: one-sided (Hestenes) Jacobi on W = B V.  Each
+// round applies 32 disjoint plane rotations to pairs of columns of W and V (a round-robin
+// schedule over 64 indices: 63 rounds per sweep, every pair once), warp w taking pair w: the
+// warp forms alpha = |W_p|^2, beta = |W_q|^2 and gamma = W_p . W_q with shuffles and rotates
+// both columns so that W_p . W_q = 0 (J. Demmel, K. Veselic, "Jacobi's method is more accurate
+// than QR", SIAM J. Matrix Anal. Appl. 1992).  One CTA barrier per round.  A pair is rotated
+// while |gamma| > 1e-6 sqrt(alpha beta); the solver stops after a sweep that rotates nothing,
+// or after max_sweeps (then NOT_CONVERGED, when a status word is given).  At convergence W's
+// columns are B's eigenvectors scaled by the eigenvalues: evals[c] = |W_c| with the sign of
+// V_c . W_c, descending (ties by index); V's column c is the eigenvector of evals[c].
 // =====================================================================================
 constexpr int kJ32Threads = 1024;
 
-// 64 x 64 only (k = 64): warp w takes pair w of each round (a round-robin schedule over 64
-// indices: 63 rounds of 32 disjoint pairs), every lane computes the pair's rotation and handles
-// entries lane and lane + 32 of the two rows, then of the two columns and of V.
 __global__ void __launch_bounds__(kJ32Threads) k_jacobi32(const float *__restrict__ B, float *__restrict__ evals,
                                                           float *__restrict__ Vout, int max_sweeps, int *status,
                                                           const int *skip) {
   if (skip && *skip) return;
-  __shared__ float A[kK][kK + 1], V[kK][kK + 1];
-  __shared__ int rotated;
+  __shared__ float W[kK][kK + 1], V[kK][kK + 1];
+  __shared__ float ev_sh[kK];
+  __shared__ int rot[2];   // per sweep parity: whether the sweep rotated anything
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   for (int idx = tid; idx < kK * kK; idx += kJ32Threads) {
     const int i = idx >> 6, j = idx & 63;
-    A[i][j] = 0.5f * (B[i * kK + j] + B[j * kK + i]);
+    W[i][j] = 0.5f * (B[i * kK + j] + B[j * kK + i]);
     V[i][j] = (i == j) ? 1.0f : 0.0f;
   }
+  if (tid < 2) rot[tid] = 0;
   __syncthreads();
   int sweep = 0;
+  bool converged = false;
   for (; sweep < max_sweeps; ++sweep) {
-    if (tid == 0) rotated = 0;
-    __syncthreads();
     for (int r = 0; r < kK - 1; ++r) {
       const int a = (w == 0) ? kK - 1 : (r + w) % (kK - 1);
       const int b = (w == 0) ? r : (r - w + (kK - 1)) % (kK - 1);
       const int p = min(a, b), q = max(a, b);
-      const float apq = A[p][q], app = A[p][p], aqq = A[q][q];
-      float c = 1.0f, s = 0.0f;
-      const bool rot = fabsf(apq) > fmaxf(1e-6f * sqrtf(fabsf(app * aqq)), 0x1p-21f * fmaxf(fabsf(app), fabsf(aqq)));
-      if (rot) {
-        const float theta = (aqq - app) / (2.0f * apq);
-        const float t = (theta >= 0.0f ? 1.0f : -1.0f) / (fabsf(theta) + sqrtf(theta * theta + 1.0f));
-        c = 1.0f / sqrtf(t * t + 1.0f);
-        s = t * c;
-      }
-      __syncthreads();   // every warp has read its pair before any row changes
-      if (rot) {
+      const float wp0 = W[l][p], wp1 = W[l + 32][p], wq0 = W[l][q], wq1 = W[l + 32][q];
+      float al = fmaf(wp0, wp0, wp1 * wp1), be = fmaf(wq0, wq0, wq1 * wq1), ga = fmaf(wp0, wq0, wp1 * wq1);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {   // rows p and q
-          const int j = l + 32 * h;
-          const float ap = A[p][j], aq = A[q][j];
-          A[p][j] = c * ap - s * aq;
-          A[q][j] = s * ap + c * aq;
-        }
+      for (int o = 16; o > 0; o >>= 1) {
+        al += __shfl_xor_sync(0xFFFFFFFFu, al, o);
+        be += __shfl_xor_sync(0xFFFFFFFFu, be, o);
+        ga += __shfl_xor_sync(0xFFFFFFFFu, ga, o);
       }
-      __syncthreads();
-      if (rot) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {   // columns p and q, and V
-          const int i = l + 32 * h;
-          const float ap = A[i][p], aq = A[i][q];
-          A[i][p] = c * ap - s * aq;
-          A[i][q] = s * ap + c * aq;
-          const float vp = V[i][p], vq = V[i][q];
-          V[i][p] = c * vp - s * vq;
-          V[i][q] = s * vp + c * vq;
-        }
-        __syncwarp();
-        if (l == 0) {
-          A[p][q] = 0.0f;
-          A[q][p] = 0.0f;
-          rotated = 1;
-        }
+      if (fabsf(ga) > 1e-6f * sqrtf(al * be) && ga != 0.0f) {   // the same decision in every lane
+        const float zeta = (be - al) / (2.0f * ga);
+        const float t = (zeta >= 0.0f ? 1.0f : -1.0f) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.0f)));
+        const float c = 1.0f / sqrtf(fmaf(t, t, 1.0f)), s = t * c;
+        W[l][p] = c * wp0 - s * wq0;
+        W[l][q] = s * wp0 + c * wq0;
+        W[l + 32][p] = c * wp1 - s * wq1;
+        W[l + 32][q] = s * wp1 + c * wq1;
+        const float vp0 = V[l][p], vp1 = V[l + 32][p], vq0 = V[l][q], vq1 = V[l + 32][q];
+        V[l][p] = c * vp0 - s * vq0;
+        V[l][q] = s * vp0 + c * vq0;
+        V[l + 32][p] = c * vp1 - s * vq1;
+        V[l + 32][q] = s * vp1 + c * vq1;
+        if (l == 0) rot[sweep & 1] = 1;
       }
+      // the next sweep's flag: every thread read it (as the previous sweep's) before round 0's
+      // barrier, and nothing sets it before the next sweep
+      if (r == 1 && tid == 0) rot[(sweep + 1) & 1] = 0;
       __syncthreads();
     }
-    if (!rotated) break;   // a whole sweep found every pair below the threshold
+    if (!rot[sweep & 1]) {
+      converged = true;
+      break;
+    }
   }
-  if (tid == 0 && sweep >= max_sweeps && status) set_status(status, GIFT_ERR_NOT_CONVERGED);
+  if (tid == 0 && !converged && status) set_status(status, GIFT_ERR_NOT_CONVERGED);
+  if (w < 2) {   // eigenvalue of column c = tid: |W_c| with the sign of V_c . W_c
+    const int c = tid;
+    float nn = 0.0f, dv = 0.0f;
+    for (int i = 0; i < kK; ++i) {
+      nn = fmaf(W[i][c], W[i][c], nn);
+      dv = fmaf(V[i][c], W[i][c], dv);
+    }
+    ev_sh[c] = (dv < 0.0f) ? -sqrtf(nn) : sqrtf(nn);
+  }
+  __syncthreads();
   if (tid < kK) {   // descending, ties by index
     const int i = tid;
-    const float e = A[i][i];
+    const float e = ev_sh[i];
     int pos = 0;
     for (int j = 0; j < kK; ++j) {
-      const float f = A[j][j];
+      const float f = ev_sh[j];
       pos += (f > e) || (f == e && j < i);
     }
     evals[pos] = e;
@@ -290,35 +297,41 @@ __global__ void __launch_bounds__(kJ32Threads) k_jacobi32(const float *__restric
 }
 
 // =====================================================================================
-// out = X M (X: d x 64 row-major, M: 64 x 64); one warp per row, lanes c and c + 32.  A warp
-// reads its whole row before it writes, so out may be X.
+// out = X L^-T (X: d x 64 row-major, L: 64 x 64 lower-triangular), i.e. the solution q of
+// L q^T = x^T for every row x, by forward substitution: one warp per row, lane l holding
+// entries l and l + 32; step c takes q_c from its lane and removes it from the later entries.
+// A warp reads its whole row before it writes, so out may be X.
 // =====================================================================================
-__global__ void __launch_bounds__(256) k_right_mul64(const float *X, int d, const float *__restrict__ M, float *out,
-                                                     const int *skip) {
+__global__ void __launch_bounds__(256) k_right_trsm64(const float *X, int d, const float *__restrict__ Lm,
+                                                      float *out, const int *skip) {
   if (skip && *skip) return;
-  __shared__ float sm[kK][kK + 1];
-  for (int idx = threadIdx.x; idx < kK * kK; idx += blockDim.x) sm[idx / kK][idx % kK] = M[idx];
+  __shared__ float Ls[kK][kK + 1];
+  __shared__ float rd[kK];
+  for (int idx = threadIdx.x; idx < kK * kK; idx += blockDim.x) Ls[idx / kK][idx % kK] = Lm[idx];
+  __syncthreads();
+  if (threadIdx.x < kK) rd[threadIdx.x] = 1.0f / Ls[threadIdx.x][threadIdx.x];
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < d; row += warps) {
-    const float x0 = X[(size_t)row * kK + lane], x1 = X[(size_t)row * kK + 32 + lane];
-    float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 8
+    float acc0 = X[(size_t)row * kK + lane], acc1 = X[(size_t)row * kK + 32 + lane];
+    float q0 = 0.0f, q1 = 0.0f;
+#pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const float xc = __shfl_sync(0xFFFFFFFFu, x0, c);
-      a0 = fmaf(xc, sm[c][lane], a0);
-      a1 = fmaf(xc, sm[c][32 + lane], a1);
+      const float qc = __shfl_sync(0xFFFFFFFFu, acc0, c) * rd[c];   // lane c's entry is final
+      if (lane == c) q0 = qc;
+      if (lane > c) acc0 = fmaf(-qc, Ls[lane][c], acc0);
+      acc1 = fmaf(-qc, Ls[32 + lane][c], acc1);
     }
-#pragma unroll 8
-    for (int c = 0; c < 32; ++c) {
-      const float xc = __shfl_sync(0xFFFFFFFFu, x1, c);
-      a0 = fmaf(xc, sm[32 + c][lane], a0);
-      a1 = fmaf(xc, sm[32 + c][32 + lane], a1);
+#pragma unroll
+    for (int c = 32; c < 64; ++c) {
+      const float qc = __shfl_sync(0xFFFFFFFFu, acc1, c - 32) * rd[c];
+      if (lane == c - 32) q1 = qc;
+      if (lane > c - 32) acc1 = fmaf(-qc, Ls[32 + lane][c], acc1);
     }
     __syncwarp();
-    out[(size_t)row * kK + lane] = a0;
-    out[(size_t)row * kK + 32 + lane] = a1;
+    out[(size_t)row * kK + lane] = q0;
+    out[(size_t)row * kK + 32 + lane] = q1;
   }
 }
 
@@ -500,9 +513,9 @@ cudaError_t launch_gram_tall(const Launch &L, const float *X, const float *Y, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_chol_rinv32(const Launch &L, const float *G, int k, float *Rinv, const int *skip) {
+cudaError_t launch_chol32(const Launch &L, const float *G, int k, float *Lout, const int *skip) {
   if (k != kK) return cudaErrorInvalidValue;
-  k_chol_rinv32<<<1, 256, 0, L.stream>>>(G, Rinv, skip);
+  k_chol32<<<1, 256, 0, L.stream>>>(G, Lout, skip);
   return cudaGetLastError();
 }
 
@@ -513,10 +526,11 @@ cudaError_t launch_jacobi32(const Launch &L, const float *B, int k, float *evals
   return cudaGetLastError();
 }
 
-cudaError_t launch_right_mul64(const Launch &L, const float *X, int d, const float *M, float *out, const int *skip) {
+cudaError_t launch_right_trsm64(const Launch &L, const float *X, int d, const float *Lm, float *out,
+                                const int *skip) {
   int grid = (d + 7) / 8;
   if (grid > 4 * L.sms) grid = 4 * L.sms;
-  k_right_mul64<<<grid, 256, 0, L.stream>>>(X, d, M, out, skip);
+  k_right_trsm64<<<grid, 256, 0, L.stream>>>(X, d, Lm, out, skip);
   return cudaGetLastError();
 }
 

@@ -184,12 +184,14 @@ cudaError_t launch_gram_tall(const Launch &L, const float *X, const float *Y, in
 // tr(a^T a / T) from the activations; part holds nparts doubles (one per CTA)
 cudaError_t launch_trace_acts32(const Launch &L, const void *a, bool bf16, int T, int d, double *part, int nparts,
                                 double *tr);
-cudaError_t launch_chol_rinv32(const Launch &L, const float *G, int k, float *Rinv, const int *skip);
+// G = L L^T (k = 64); L lower-triangular, upper part zero
+cudaError_t launch_chol32(const Launch &L, const float *G, int k, float *Lout, const int *skip);
 // at most max_sweeps sweeps; report: NOT_CONVERGED into the status word when they run out
 cudaError_t launch_jacobi32(const Launch &L, const float *B, int k, float *evals, float *V, int max_sweeps,
                             bool report, const int *skip);
-// out = X M for X d x 64 and M 64 x 64 (out may be X)
-cudaError_t launch_right_mul64(const Launch &L, const float *X, int d, const float *M, float *out, const int *skip);
+// out = X L^-T for X d x 64 and L 64 x 64 lower-triangular (out may be X)
+cudaError_t launch_right_trsm64(const Launch &L, const float *X, int d, const float *Lm, float *out,
+                                const int *skip);
 // Y <- Y V in place with the Ritz residuals' partial sums of squares (ritz_rotate_ctas x 64
 // floats), then the convergence flag from them
 int ritz_rotate_ctas(int sms, int d);

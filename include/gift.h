@@ -198,7 +198,7 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
  *           into BF16 terms, one fresh FP32 accumulator per 64-deep chunk): each power step
  *           forms Y = A Q (by default as a^T (a Q) / T, A never formed; GIFT_OPT_SKETCH
  *           selects the explicit product) and re-orthonormalises Q by CholQR2 with
- *           compensated FP32 Gram sums; Rayleigh-Ritz steps (FP32 parallel Jacobi) rotate
+ *           compensated FP32 Gram sums; Rayleigh-Ritz steps (FP32 one-sided Jacobi) rotate
  *           Q on the first two steps and every fourth, and stop the iteration once each of
  *           the top `rank` Ritz pairs has a residual ||A u - theta u|| <= 1e-4 theta (at
  *           most GIFT_OPT_SUBSPACE_ITERS steps, default 16).  The last Rayleigh-Ritz step takes
