@@ -1219,6 +1219,40 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
   return GIFT_OK;
 }
 
+gift_status gift_boundary_hit_rates(gift_ctx *ctx, int n_tensors, const float *const *W, const int *d_out,
+                                    const int *d_in, gift_format fmt, gift_scaling scaling,
+                                    unsigned long long *d_counts, void *ws, size_t ws_bytes, int *d_status,
+                                    cudaStream_t stream) {
+  if (!ctx || !W || !d_out || !d_in || !d_counts || n_tensors < 1) return GIFT_ERR_INVALID_ARG;
+  if (fmt != GIFT_FMT_E4M3 && fmt != GIFT_FMT_E5M2) return GIFT_ERR_INVALID_ARG;
+  if (!valid_scaling(scaling)) return GIFT_ERR_INVALID_ARG;
+  for (int t = 0; t < n_tensors; ++t)   // every tensor is checked before anything is enqueued
+    if (!W[t] || d_out[t] <= 0 || d_in[t] <= 0) return GIFT_ERR_INVALID_ARG;
+  if (scaling != GIFT_SCALE_TENSOR) {   // the block scalings need no amax pass
+    for (int t = 0; t < n_tensors; ++t) {
+      const gift_status st = gift_boundary_hit_rate(ctx, W[t], d_out[t], d_in[t], fmt, scaling, d_counts + 3 * t,
+                                                    ws, ws_bytes, d_status, stream);
+      if (st != GIFT_OK) return st;
+    }
+    return GIFT_OK;
+  }
+  const CodecWs need = codec_layout(nullptr, ctx->sms, GIFT_OP_AMAX, GIFT_XF_IDENTITY, 1, 1);
+  if (!ws || ws_bytes < need.bytes) return GIFT_ERR_INVALID_ARG;
+  const CodecWs w = codec_layout(ws, ctx->sms, GIFT_OP_AMAX, GIFT_XF_IDENTITY, 1, 1);
+  const Launch L = mk(ctx, d_status, stream);
+  for (int t0 = 0; t0 < n_tensors; t0 += kMaxReplicas) {   // the 64 amax words of the workspace
+    const int m = (n_tensors - t0 < kMaxReplicas) ? n_tensors - t0 : kMaxReplicas;
+    HitsArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int t = 0; t < m; ++t) {
+      a.x[t] = W[t0 + t];
+      a.n[t] = (size_t)d_out[t0 + t] * d_in[t0 + t];
+    }
+    CK(launch_hits_multi(L, fmt, a, m, reinterpret_cast<uint32_t *>(w.amax), d_counts + 3 * (size_t)t0));
+  }
+  return GIFT_OK;
+}
+
 // Fragile-layer selection from a profiling window (host only).  Scores are formed in double
 // from the integer counts, so every comparison below is exact and repeatable.
 gift_status gift_select_fragile(int L, const unsigned long long *counts, int k, int k_min, int k_max, int *order,

@@ -39,7 +39,16 @@ struct MultiArgs {
   uint32_t *amax_bits[kMaxReplicas];   // amax: max-accumulated |x| bit pattern of each tensor
 };
 
+// Tensors of any sizes for one multi-tensor launch (the profiler's batched hit counts).
+struct HitsArgs {
+  const float *x[kMaxReplicas];
+  size_t n[kMaxReplicas];
+};
+
 // ---- quant.cu ---------------------------------------------------------------------------
+// amax words zeroed, every tensor's amax, then every tensor's hits added into counts[3 t ..]
+cudaError_t launch_hits_multi(const Launch &L, int fmt, const HitsArgs &a, int T, uint32_t *amax_bits,
+                              unsigned long long *counts);
 cudaError_t launch_amax(const Launch &L, const float *x, const float *r, size_t n, float *amax_accum);
 cudaError_t launch_pack_tensor(const Launch &L, int fmt, const float *x, float *r, size_t n, const float *amax,
                                uint8_t *codes, float *scale, float *amax_out, float *tout);

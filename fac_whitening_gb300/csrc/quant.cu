@@ -234,6 +234,86 @@ __global__ void __launch_bounds__(256) k_pack_tensor_multi(MultiArgs a, int R, s
 }
 
 // =====================================================================================
+// Boundary hits of several tensors of any sizes (the profiler over a model's layers): one
+// launch takes every tensor's amax, one launch counts every tensor's hits with its own scale,
+// the tensors taken last to first so that the count reads first what the amax pass read last.
+// Per tensor the arithmetic is that of k_amax + k_hits_tensor.
+// =====================================================================================
+__global__ void __launch_bounds__(256) k_amax_multi_var(HitsArgs a, int T, uint32_t *amax_bits, int *status) {
+  __shared__ uint32_t red[8];
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (int t = 0; t < T; ++t) {
+    const float *x = a.x[t];
+    const size_t n = a.n[t];
+    uint32_t m = 0;
+    size_t done = 0;
+    if ((((uintptr_t)x) & 15u) == 0) {
+      m = amax_pass(reinterpret_cast<const float4 *>(x), n >> 2, tid, stride);
+      done = (n >> 2) << 2;
+    }
+    for (size_t i = done + tid; i < n; i += stride) m = max(m, abs_bits(x[i]));
+    m = block_max_u32<256>(m, red);
+    if (threadIdx.x == 0) {
+      if (m) atomicMax(amax_bits + t, m);
+      if (m >= 0x7F800000u) set_status(status, GIFT_ERR_NONFINITE);
+    }
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(256) k_hits_multi_var(HitsArgs a, int T, const uint32_t *__restrict__ amax_bits,
+                                                        unsigned long long *__restrict__ counts) {
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (int t = T - 1; t >= 0; --t) {
+    const float *x = a.x[t];
+    const size_t n = a.n[t];
+    const ScalePair sp = scale_pair(__uint_as_float(amax_bits[t]), fmax_of<F>());
+    uint32_t up = 0, lo = 0;
+    auto tally4 = [&](const float4 &v) {
+      const uint32_t c = pack4_fp8<F>(__fmul_rn(v.x, sp.m), __fmul_rn(v.y, sp.m), __fmul_rn(v.z, sp.m),
+                                      __fmul_rn(v.w, sp.m));
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t mag = (c >> (8 * e)) & 0x7Fu;
+        up += (mag == maxcode_of<F>());
+        lo += (mag == 0u && vv[e] != 0.0f);
+      }
+    };
+    size_t done = 0;
+    if ((((uintptr_t)x) & 15u) == 0) {
+      const float4 *x4 = reinterpret_cast<const float4 *>(x);
+      const size_t n4 = n >> 2;
+      size_t i = tid;
+      for (; i + 7 * stride < n4; i += 8 * stride) {   // eight loads in flight
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcs(x4 + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) tally4(v[u]);
+      }
+      for (; i < n4; i += stride) tally4(__ldcs(x4 + i));
+      done = n4 << 2;
+    }
+    for (size_t i = done + tid; i < n; i += stride) {
+      const float v = x[i];
+      const uint32_t mag = pack1_fp8<F>(__fmul_rn(v, sp.m)) & 0x7Fu;
+      up += (mag == maxcode_of<F>());
+      lo += (mag == 0u && v != 0.0f);
+    }
+    up = warp_add_u32(up);
+    lo = warp_add_u32(lo);
+    if ((threadIdx.x & 31) == 0) {
+      if (up) atomicAdd(counts + 3 * (size_t)t + 0, (unsigned long long)up);
+      if (lo) atomicAdd(counts + 3 * (size_t)t + 1, (unsigned long long)lo);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(counts + 3 * (size_t)t + 2, (unsigned long long)n);
+  }
+}
+
+// =====================================================================================
 // The replicas of one tensor encoded with one shared scale (the synchronised scale of the
 // Euclidean path: the max over the replicas of their amax) in one cooperative launch: the
 // amax pass over every replica, a grid-wide barrier, then the pack of every replica with the
@@ -1127,6 +1207,20 @@ cudaError_t launch_block512(const Launch &L, int fmt, int mode, const float *x, 
     else if (mode == 1) block512_launch<FMT_E5M2, 1>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
     else block512_launch<FMT_E5M2, 2>(L, vec, x, r, n, amax_in, codes, scales, amax_out, tout, counts);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hits_multi(const Launch &L, int fmt, const HitsArgs &a, int T, uint32_t *amax_bits,
+                              unsigned long long *counts) {
+  size_t nmax = 0;
+  for (int t = 0; t < T; ++t) nmax = a.n[t] > nmax ? a.n[t] : nmax;
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, (size_t)T * sizeof(uint32_t), L.stream);
+  if (e != cudaSuccess) return e;
+  const int grid = stream_grid(L, (nmax + 3) / 4, 1024);
+  k_amax_multi_var<<<grid, 256, 0, L.stream>>>(a, T, amax_bits, L.status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (fmt == GIFT_FMT_E4M3) k_hits_multi_var<FMT_E4M3><<<grid, 256, 0, L.stream>>>(a, T, amax_bits, counts);
+  else k_hits_multi_var<FMT_E5M2><<<grid, 256, 0, L.stream>>>(a, T, amax_bits, counts);
   return cudaGetLastError();
 }
 

@@ -68,6 +68,8 @@ def _declare(lib):
         "gift_factor_update_from_kfac": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _vp, ctypes.c_uint64, _i, _vp,
                                               _sz, _vp, _vp]),
         "gift_kfac_factor": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _vp]),
+        "gift_boundary_hit_rates": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_i), ctypes.POINTER(_i), _i,
+                                         _i, _vp, _vp, _sz, _vp, _vp]),
         "gift_factor_planes_bytes": (_sz, [_i]),
         "gift_factor_prepare": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp]),
         "gift_amax": (_i, [_vp, ctypes.POINTER(GiftFactor), _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -381,6 +383,18 @@ def gift_boundary_hit_rate(ctx: Context, W, fmt: str, scaling: str, counts, ws=N
     _check(lib().gift_boundary_hit_rate(ctx.handle, _p(W), d_out, d_in, FMT[fmt], SCALING[scaling], _p(counts),
                                         _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
                                         _stream(stream)), "gift_boundary_hit_rate")
+
+
+def gift_boundary_hit_rates(ctx: Context, Ws: Sequence, fmt: str, scaling: str, counts, ws=None, status=None,
+                            stream=None):
+    """Hit counts of several tensors in one call; counts is an n x 3 int64 device tensor."""
+    n = len(Ws)
+    ptrs = (_vp * n)(*[_p(W) for W in Ws])
+    rows = (_i * n)(*[int(W.shape[0]) for W in Ws])
+    cols = (_i * n)(*[int(W.shape[1]) for W in Ws])
+    _check(lib().gift_boundary_hit_rates(ctx.handle, n, ptrs, rows, cols, FMT[fmt], SCALING[scaling], _p(counts),
+                                         _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+                                         _stream(stream)), "gift_boundary_hit_rates")
 
 
 def gift_encode_lowrank_noalloc(ctx: Context, f: Factor, W, fmt: str, codes, scales, amax_in=None, amax_out=None,

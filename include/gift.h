@@ -405,6 +405,23 @@ gift_status gift_boundary_hit_rate(gift_ctx *ctx, const float *W, int d_out, int
                                    unsigned long long *d_counts, void *ws, size_t ws_bytes,
                                    int *d_status, cudaStream_t stream);
 
+/* The boundary-hit profiler over several tensors in one call (the profiling window's pass over
+ * a model's layers): for each tensor t the counts gift_boundary_hit_rate would add, added into
+ * d_counts[3 t .. 3 t + 2].  No counterpart in the pages beyond the per-tensor procedure; it
+ * exists so that a model's layers take two launches (every tensor's amax, then every tensor's
+ * counts) instead of two or three each.
+ *  W, d_out, d_in : host arrays of n_tensors device pointers and shapes (FP32, row-major).
+ *  d_counts       : device, n_tensors x 3 unsigned 64-bit, added into.
+ *  ws             : gift_workspace_bytes(GIFT_OP_AMAX, IDENTITY, ..., 1, 1, ...) bytes (64
+ *                   amax words: tensors are taken 64 at a time); per-tensor calls for the
+ *                   block scalings.
+ * Returns INVALID_ARG on any null pointer or shape <= 0 (nothing enqueued).  d_status:
+ * NONFINITE. */
+gift_status gift_boundary_hit_rates(gift_ctx *ctx, int n_tensors, const float *const *W, const int *d_out,
+                                    const int *d_in, gift_format fmt, gift_scaling scaling,
+                                    unsigned long long *d_counts, void *ws, size_t ws_bytes, int *d_status,
+                                    cudaStream_t stream);
+
 /* Fragile-layer selection after a profiling window ([notes] simplification 3: boundary-hit
  * rates averaged over the profiling window, upper and lower rates summed into a fragility
  * score; the geometry-aware branch goes to the layers before the clear drop in that score).

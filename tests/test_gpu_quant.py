@@ -239,3 +239,29 @@ def test_encode_block512_unaligned_and_transforms():
     with pytest.raises(G.GiftError) as e:
         encode(f, W, "e4m3", "block512")
     assert e.value.status == G.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("scaling", ["tensor", "block128"])
+def test_boundary_hits_batched(fmt, scaling):
+    # one call over tensors of different sizes (aligned, unaligned, a 1-element tensor, an
+    # all-zero tensor, more than 64 tensors) gives exactly the per-tensor counts, and the oracle's
+    rng = np.random.default_rng(31)
+    shapes = [(300, 1024), (1, 1), (17, 33), (64, 256), (8, 8)] * 14   # 70 tensors
+    Ws = [t(rng.standard_t(3, size=s).astype(np.float32) * np.exp(rng.normal(0, 2, size=(1, s[1]))).astype(np.float32))
+          for s in shapes]
+    Ws[4] = torch.zeros(8, 8, device=DEV)
+    n = len(Ws)
+    got = torch.zeros(n, 3, dtype=torch.int64, device=DEV)
+    want = torch.zeros(n, 3, dtype=torch.int64, device=DEV)
+    w = ws("amax", "identity", fmt, "tensor", 1, 1)
+    st = status()
+    G.gift_boundary_hit_rates(ctx(), Ws, fmt, scaling, got, ws=w, status=st)
+    for i, W in enumerate(Ws):
+        G.gift_boundary_hit_rate(ctx(), W, fmt, scaling, want[i], ws=w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(got, want)
+    for i in (0, 2, 4):
+        up, lo, cnt = O.boundary_hits(Ws[i].cpu().numpy(), fmt, scaling)
+        assert got[i].tolist() == [up, lo, cnt]
