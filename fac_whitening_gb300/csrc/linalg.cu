@@ -423,13 +423,19 @@ __global__ void __launch_bounds__(256) k_chol_inv_small(double *A, int lda, doub
     if (tid > j && tid < n) S[tid][j] *= rp;            // column j of L
     if (tid < 64 && tid <= j) X[j][tid] *= rp;         // row j of L^-1
     __syncthreads();
-    const int rows = n - j - 1;
-    for (int idx = tid; idx < rows * n; idx += 256) {
-      const int i = j + 1 + idx / n, c = idx - (idx / n) * n;
-      if (c > i) continue;
-      const double lij = S[i][j];
-      if (c > j) S[i][c] = fma(-lij, S[c][j], S[i][c]);
-      else X[i][c] = fma(-lij, X[j][c], X[i][c]);
+    // thread t: column t % 64 of rows j + 1 + t / 64, then every fourth row, from the first
+    // row that has the column (c <= i)
+    const int c = tid & 63;
+    if (c < n) {
+      const bool upd_s = c > j;
+      const double pivc = upd_s ? S[c][j] : X[j][c];
+      int i = j + 1 + (tid >> 6);
+      if (i < c) i += ((c - i + 3) >> 2) << 2;
+      for (; i < n; i += 4) {
+        const double lij = S[i][j];
+        if (upd_s) S[i][c] = fma(-lij, pivc, S[i][c]);
+        else X[i][c] = fma(-lij, pivc, X[i][c]);
+      }
     }
     __syncthreads();
   }

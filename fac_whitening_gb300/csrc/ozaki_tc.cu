@@ -25,9 +25,10 @@
 // representable in FP32, so the tensor core's FP32 accumulation of it is exact whatever its
 // internal order.  The epilogue converts each level's chunk sum to an integer and adds it to
 // 32-bit integer accumulators (exact for K <= 8192), and only at the end of the tile combines
-// the seven levels in FP64 with their weights and the row and column scales: the result is the
-// product of the sliced operands up to one FP64 rounding per level, and the slicing itself
-// keeps 56 bits of every operand relative to its row maximum.
+// the seven levels (as two exact 64-bit fixed-point integers, converted to FP64 and added with
+// one FMA) and applies the row and column scales (exact powers of two): the result is the
+// product of the sliced operands up to a few FP64 roundings, and the slicing itself keeps 56
+// bits of every operand relative to its row maximum.
 //
 //   k_oz_rowmax   max |x| of every row of op(A) or op(B)^T (bit patterns, atomicMax)
 //   k_oz_slices   the seven digit planes (BF16, the blocked layout of gemm_tc.cu: every
@@ -78,10 +79,19 @@ struct OzParams {
   const unsigned long long *rmA, *rmB;   // row maxima (bit patterns of |x|)
 };
 
-// The row's scale exponent: the smallest e with max |x| < 2^e (0 for an all-zero row).
+// The row's scale exponent: the smallest e with max |x| < 2^e (0 for an all-zero row), from
+// the bit pattern of the maximum (integer arithmetic; subnormal maxima take the library path).
 __device__ __forceinline__ int oz_exp(unsigned long long bits) {
+  const int ex = (int)((bits >> 52) & 0x7FF);
+  if (ex) return ex - 1022;   // 2^(ex-1023) <= m < 2^(ex-1022)
   const double m = __longlong_as_double((long long)bits);
   return (m == 0.0) ? 0 : ilogb(m) + 1;
+}
+
+// 2^e as a double (exact), from the exponent bits where e is a normal exponent.
+__device__ __forceinline__ double oz_pow2(int e) {
+  if (e >= -1022 && e <= 1023) return __longlong_as_double((long long)(e + 1023) << 52);
+  return ldexp(1.0, e);
 }
 
 template <bool TRANS>
@@ -335,10 +345,13 @@ __global__ void __launch_bounds__(kOzThreads, 1) k_gemm_oz(const __grid_constant
         for (int j = 0; j < 16; ++j) {
           const int cn = tn * kOzN + 16 * half + j;
           if (cn >= P.N) continue;
-          double v = 0.0;
-#pragma unroll
-          for (int l = kOzS - 1; l >= 0; --l) v += scalbn((double)acc[l][j], -8 * (l + 2));   // smallest first
-          v = scalbn(v, ea + oz_exp(P.rmB[cn]));
+          // levels 0-3 and 4-6 as two exact 64-bit fixed-point integers (level l weighs
+          // 2^{-8(l+2)}: hi in units of 2^-40, lo in units of 2^-64), then two conversions and
+          // one FMA: the FP64 units of this GPU are slow, the integer ones are not
+          const long long hi = ((long long)acc[0][j] << 24) + ((long long)acc[1][j] << 16) +
+                               ((long long)acc[2][j] << 8) + (long long)acc[3][j];
+          const long long lo = ((long long)acc[4][j] << 16) + ((long long)acc[5][j] << 8) + (long long)acc[6][j];
+          const double v = fma((double)hi, 0x1p-40, (double)lo * 0x1p-64) * oz_pow2(ea + oz_exp(P.rmB[cn]));
           crow[cn] = (P.beta == 0.0) ? P.alpha * v : fma(P.alpha, v, P.beta * crow[cn]);
         }
       }
