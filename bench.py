@@ -400,13 +400,21 @@ def main_gift(args):
 
     solo_mode = [False]
 
-    def fork_join(items, fn):
+    # The layers' decodes are latency-bound one by one: they run side by side, each stream's
+    # context sized for its share of the SMs (GIFT_OPT_SMS), with workspaces sized by it.
+    ctx_q = G.Context(local)
+    G.gift_set_option(ctx_q, G.OPT_SMS, max(1, torch.cuda.get_device_properties(dev).multi_processor_count // nstr))
+    wsq = [torch.zeros(max(G.gift_workspace_bytes(ctx_q, "decode", "lowrank", FMT, "tensor", d_out, d_in), 256),
+                       dtype=torch.uint8, device=dev) for _ in range(nstr)]
+
+    def fork_join(items, fn, ws_list=None):
         """Run fn(item, ws) for independent items round-robin over the side streams; the
         current stream waits for all of them (one join per stage group).  In solo mode the
         items run back to back on the current stream (per-call timing)."""
+        ws_list = wss if ws_list is None else ws_list
         if solo_mode[0]:
             for it in items:
-                fn(it, wss[0])
+                fn(it, ws_list[0])
             return
         main = torch.cuda.current_stream()
         start = torch.cuda.Event()
@@ -415,7 +423,7 @@ def main_gift(args):
             s.wait_stream(main)
         for i, it in enumerate(items):
             with torch.cuda.stream(streams[i % nstr]):
-                fn(it, wss[i % nstr])
+                fn(it, ws_list[i % nstr])
         for s in streams:
             main.wait_stream(s)
 
@@ -434,8 +442,8 @@ def main_gift(args):
 
     def g_decode():
         fork_join(list(zip(factors, gl)),
-                  lambda it, w: G.gift_decode(ctx, it[0], it[1]["avg"], False, "f32", "tensor", d_out, d_in,
-                                              it[1]["out"], ws=w, status=st))
+                  lambda it, w: G.gift_decode(ctx_q, it[0], it[1]["avg"], False, "f32", "tensor", d_out, d_in,
+                                              it[1]["out"], ws=w, status=st), ws_list=wsq)
 
     def euclid_encode(E, w):
         # the R replicas' shared amax and their pack with it: one cooperative launch

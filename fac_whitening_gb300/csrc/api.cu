@@ -321,6 +321,7 @@ gift_status gift_create(gift_ctx **ctx, int device) {
   gift_ctx *c = static_cast<gift_ctx *>(std::malloc(sizeof(gift_ctx)));
   if (!c) return GIFT_ERR_CUDA;
   c->device = device;
+  c->device_sms = sms;
   c->sms = sms;
   c->subspace_iters = 16;
   c->barrier_wait = kDefaultBarrierWait;
@@ -346,6 +347,11 @@ gift_status gift_set_option(gift_ctx *ctx, gift_option opt, long long value) {
   if (opt == GIFT_OPT_BARRIER_WAIT) {
     if (value < 0 || value > 20000000000LL) return GIFT_ERR_INVALID_ARG;
     ctx->barrier_wait = value;
+    return GIFT_OK;
+  }
+  if (opt == GIFT_OPT_SMS) {
+    if (value < 1 || value > ctx->device_sms) return GIFT_ERR_INVALID_ARG;
+    ctx->sms = (int)value;
     return GIFT_OK;
   }
   return GIFT_ERR_INVALID_ARG;

@@ -6,7 +6,8 @@
 // Host context behind the opaque gift_ctx handle.
 struct gift_ctx {
   int device;
-  int sms;
+  int device_sms;           // SMs of the device
+  int sms;                  // SMs this context's launches size their grids for (<= device_sms)
   int subspace_iters;
   long long barrier_wait;   // clock cycles a CTA waits at a streaming grid barrier
   int sketch;               // rank-r refresh: 0 implicit a^T (a Q) / T, 1 explicit A Q

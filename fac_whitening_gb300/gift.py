@@ -29,6 +29,7 @@ OP = {"factor_update": 0, "encode": 1, "decode": 2, "amax": 3, "kfac_factor": 4,
 OPT_SUBSPACE_ITERS = 0
 OPT_BARRIER_WAIT = 1
 OPT_SKETCH = 2
+OPT_SMS = 3
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int

@@ -156,11 +156,17 @@ typedef enum {
                                   activations and never forms A; 1 forms A = a^T a / T (the
                                   K-FAC product) and multiplies it.  Set it before
                                   gift_workspace_bytes: the two need different workspaces. */
-  GIFT_OPT_BARRIER_WAIT = 1    /* SM clock cycles a CTA of the shared-scale encode waits at its
+  GIFT_OPT_BARRIER_WAIT = 1,   /* SM clock cycles a CTA of the shared-scale encode waits at its
                                   grid-wide barrier before it gives up, writes GIFT_ERR_TIMEOUT
                                   to d_status and stores no codes (default 2e9, about a second;
                                   0..2e10).  A small value makes the wait run out on purpose: the
                                   kernel still ends and the context stays usable. */
+  GIFT_OPT_SMS = 3             /* SMs the context's launches size their grids for (default and
+                                  maximum: the device's SM count).  With a fraction of the SMs per
+                                  context, calls on several streams run side by side on disjoint
+                                  shares of the GPU, which pays for latency-bound calls such as
+                                  one layer's decode.  Workspace sizes depend on it: set it
+                                  before gift_workspace_bytes. */
 } gift_option;
 
 /* Create a context for CUDA device `device` (queries its SM count).  Returns

@@ -288,3 +288,35 @@ def test_lowrank_block_unaligned_simt():
     np.testing.assert_array_equal(out["codes"], q["codes"])
     np.testing.assert_array_equal(out["residual"], (out["tout"].astype(np.float64) - O.dequantize_any(q, "e4m3", "block128"))
                                   .astype(np.float32))
+
+
+@pytest.mark.parametrize("sms", [38, 7])
+def test_reduced_sm_context(c3, sms):
+    # a context sized for a share of the SMs (GIFT_OPT_SMS, for calls run side by side on
+    # several streams) keeps the contract: encode within the transform tolerance with codes
+    # that quantise its own W~, decode within 1e-5 of the oracle's map back
+    Ws, F, _ = c3
+    W = Ws[0]
+    d_out, d_in = W.shape
+    cq = G.Context(torch.cuda.current_device())
+    G.gift_set_option(cq, G.OPT_SMS, sms)
+    f = factor_to_gpu("lowrank", d_out, d_in, F=F)
+    codes, scales, _ = (torch.empty(d_out * d_in, dtype=torch.uint8, device=DEV), torch.empty(1, device=DEV), None)
+    tout = torch.empty(d_out, d_in, device=DEV)
+    st = status()
+    wenc = torch.zeros(G.gift_workspace_bytes(cq, "encode", "lowrank", "e4m3", "tensor", d_out, d_in),
+                       dtype=torch.uint8, device=DEV)
+    G.gift_encode(cq, f, t(W), "e4m3", "tensor", codes, scales, transformed_out=tout, ws=wenc, status=st)
+    X = np.random.default_rng(9).standard_normal(W.shape).astype(np.float32)
+    Wo = torch.empty(d_out, d_in, device=DEV)
+    wdec = torch.zeros(G.gift_workspace_bytes(cq, "decode", "lowrank", "f32", "tensor", d_out, d_in),
+                       dtype=torch.uint8, device=DEV)
+    G.gift_decode(cq, f, t(X), False, "f32", "tensor", d_out, d_in, Wo, ws=wdec, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    tw = tout.cpu().numpy()
+    assert rel_fro(tw, O.lowrank_whiten(W, F)) <= TOL
+    np.testing.assert_array_equal(codes.cpu().numpy().reshape(W.shape), O.quantize(tw, "e4m3")["codes"])
+    assert rel_fro(Wo.cpu().numpy(), O.lowrank_unwhiten(X, F)) <= TOL
+    with pytest.raises(G.GiftError):
+        G.gift_set_option(cq, G.OPT_SMS, 100000)
