@@ -166,9 +166,14 @@ __global__ void __launch_bounds__(256) k_chol32(const float *__restrict__ G, flo
     const int c0 = 16 * p, c1 = c0 + 16;
     if (tid < 32) {
       for (int j = c0; j < c1; ++j) {
+        // 1/sqrt(d) from the hardware estimate and one Newton step, sqrt(d) = d / sqrt(d)
         const float d = S[j][j];
-        const float piv = (d > tiny) ? sqrtf(d) : 1.0f;
-        const float rp = 1.0f / piv;
+        float rp = 1.0f, piv = 1.0f;
+        if (d > tiny) {
+          const float r0 = rsqrtf(d);
+          rp = r0 * fmaf(-0.5f * d * r0, r0, 1.5f);
+          piv = d * rp;
+        }
         __syncwarp();   // every lane has read the pivot
         const int r0 = lane, r1 = lane + 32;
         if (r0 > j) S[r0][j] *= rp;
@@ -247,10 +252,13 @@ __global__ void __launch_bounds__(kJ32Threads) k_jacobi32(const float *__restric
         be += __shfl_xor_sync(0xFFFFFFFFu, be, o);
         ga += __shfl_xor_sync(0xFFFFFFFFu, ga, o);
       }
-      if (fabsf(ga) > 1e-6f * sqrtf(al * be) && ga != 0.0f) {   // the same decision in every lane
-        const float zeta = (be - al) / (2.0f * ga);
-        const float t = (zeta >= 0.0f ? 1.0f : -1.0f) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.0f)));
-        const float c = 1.0f / sqrtf(fmaf(t, t, 1.0f)), s = t * c;
+      // |gamma| > 1e-6 sqrt(alpha beta), squared (no square root on the chain); the same
+      // decision in every lane.  The rotation needs no correctly rounded roots or quotients:
+      // c and s from the hardware reciprocal square root keep c^2 + s^2 = 1 to a few ulp.
+      if (ga * ga > 1e-12f * (al * be) && ga != 0.0f) {
+        const float zeta = (be - al) * __frcp_rn(2.0f * ga);
+        const float t = copysignf(__frcp_rn(fabsf(zeta) + __fsqrt_rn(fmaf(zeta, zeta, 1.0f))), zeta);
+        const float c = rsqrtf(fmaf(t, t, 1.0f)), s = t * c;
         W[l][p] = c * wp0 - s * wq0;
         W[l][q] = s * wp0 + c * wq0;
         W[l + 32][p] = c * wp1 - s * wq1;
