@@ -353,6 +353,38 @@ def main_gift(args):
         torch.cuda.synchronize()
         refresh[prec] = fe0.elapsed_time(fe1) / len(gl)
     factor_ms = refresh.get("fp32", 0.0)
+    # all the layers refreshed together, as Algorithm 1 refreshes them every K steps: eight at a
+    # time on side streams, each with its own workspace.  The refresh's 64 x 64 steps are
+    # single-CTA dependent chains and its sketches fill the GPU; the layers' chains overlap the
+    # other layers' sketches (measured: 1, 2, 4, 8, 13 streams gave 5.67, 4.02, 3.27, 2.87,
+    # 2.88 ms per layer; quarter-GPU contexts did worse).  Scratch factors: the codec keeps
+    # the factors refreshed above.
+    if gl:
+        nrs = 8
+        rws = [torch.zeros(fws.numel(), dtype=torch.uint8, device=dev) for _ in range(nrs)]
+        rstreams = [torch.cuda.Stream() for _ in range(nrs)]
+        rscratch = [G.Factor.empty("lowrank", d_out, d_in, 32, device=dev) for _ in gl]
+
+        def refresh_all():
+            main = torch.cuda.current_stream()
+            for s_ in rstreams:
+                s_.wait_stream(main)
+            for i, L in enumerate(gl):
+                j = i % nrs
+                with torch.cuda.stream(rstreams[j]):
+                    G.gift_factor_update(ctx, rscratch[i], L["a"], seed=1000 + i, prec="fp32", ws=rws[j], status=st)
+            for s_ in rstreams:
+                main.wait_stream(s_)
+
+        refresh_all()
+        torch.cuda.synchronize()
+        fe0.record()
+        refresh_all()
+        fe1.record()
+        torch.cuda.synchronize()
+        refresh["fp32_all_layers"] = fe0.elapsed_time(fe1) / len(gl)
+        del rws, rscratch
+        torch.cuda.empty_cache()
     # the K-FAC factor alone on the tensor cores (gift_kfac_factor: transpose, tcgen05 SYRK of
     # the lower tiles, mirror), d (d + 1) T flops
     kfac = None
@@ -627,7 +659,9 @@ def main_gift(args):
                                            "activations, CUDA events): the implicit sketch a^T (a Q) / T on the "
                                            "tensor cores, CholQR2 and Rayleigh-Ritz in FP32, stopped once the Ritz "
                                            "residuals converge (at most 16 iterations); fp32 = three-term operand "
-                                           "splits (the factors the codec uses), tc = two-term"},
+                                           "splits (the factors the codec uses), tc = two-term, one layer after "
+                                           "the other on the whole GPU; fp32_all_layers = the 13 layers refreshed "
+                                           "together, eight at a time on side streams (total / 13)"},
                 "device_status": status_word}
         print(json.dumps(line), flush=True)
     if world > 1:
