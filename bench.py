@@ -340,18 +340,21 @@ def main_gift(args):
     # the codec uses the FP32-precision factors; the tensor-core (TC precision) refresh is
     # timed beside it on the same activations
     refresh = {}
+    replayed = True
     for prec in ("tc", "fp32"):
         if not gl:
             break
         scratch = [G.Factor.empty("lowrank", d_out, d_in, 32, device=dev) for _ in gl] if prec == "tc" else factors
         G.gift_factor_update(ctx, scratch[0], gl[0]["a"], seed=1, prec=prec, ws=fws, status=st)   # warm-up
         torch.cuda.synchronize()
-        fe0.record()
-        for i, L in enumerate(gl):
-            G.gift_factor_update(ctx, scratch[i], L["a"], seed=1000 + i, prec=prec, ws=fws, status=st)
-        fe1.record()
-        torch.cuda.synchronize()
-        refresh[prec] = fe0.elapsed_time(fe1) / len(gl)
+
+        def refresh_seq(scratch=scratch, prec=prec):
+            for i, L in enumerate(gl):
+                G.gift_factor_update(ctx, scratch[i], L["a"], seed=1000 + i, prec=prec, ws=fws, status=st)
+
+        ms, rep = graph_ms(refresh_seq)
+        replayed = replayed and rep
+        refresh[prec] = ms / len(gl)
     factor_ms = refresh.get("fp32", 0.0)
     # all the layers refreshed together, as Algorithm 1 refreshes them every K steps: eight at a
     # time on side streams, each with its own workspace.  The refresh's 64 x 64 steps are
@@ -378,11 +381,9 @@ def main_gift(args):
 
         refresh_all()
         torch.cuda.synchronize()
-        fe0.record()
-        refresh_all()
-        fe1.record()
-        torch.cuda.synchronize()
-        refresh["fp32_all_layers"] = fe0.elapsed_time(fe1) / len(gl)
+        ms, rep = graph_ms(refresh_all)
+        replayed = replayed and rep
+        refresh["fp32_all_layers"] = ms / len(gl)
         del rws, rscratch
         torch.cuda.empty_cache()
     # the K-FAC factor alone on the tensor cores (gift_kfac_factor: transpose, tcgen05 SYRK of
@@ -661,7 +662,10 @@ def main_gift(args):
                                            "residuals converge (at most 16 iterations); fp32 = three-term operand "
                                            "splits (the factors the codec uses), tc = two-term, one layer after "
                                            "the other on the whole GPU; fp32_all_layers = the 13 layers refreshed "
-                                           "together, eight at a time on side streams (total / 13)"},
+                                           "together, eight at a time on side streams (total / 13); each sequence "
+                                           "captured once into a CUDA graph and replayed (the refresh is a fixed "
+                                           "launch sequence)",
+                                   "graph_replay": replayed},
                 "device_status": status_word}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -671,6 +675,30 @@ def main_gift(args):
 # --------------------------------------------------------------------------------------
 # The other configurations and the fidelity per format (after the timed region)
 # --------------------------------------------------------------------------------------
+def graph_ms(fn):
+    """(ms, replayed): one run of fn timed with CUDA events, fn's launches captured once into
+    a CUDA graph and the graph replayed after one untimed replay (the host's per-launch cost
+    and the gaps between launches are not in the number); eager if the capture fails."""
+    import torch
+    run, replayed = fn, False
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        run, replayed = g.replay, True
+    except Exception:   # a call that cannot be captured: time it eagerly
+        torch.cuda.synchronize()
+    run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    run()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b), replayed
+
+
 def time_cold(fn, reps=5):
     """Mean ms of fn() over reps, each run after a 256 MB write (L2 flushed), CUDA events on
     the current stream.  fn's launches are captured once into a CUDA graph and the graph is
