@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(256) k_gram_sum(const float *__restrict__ part
 // written lower-triangular (upper part zero).  A pivot below 1e-10 of the largest diagonal (a
 // numerically rank-deficient block) is replaced by 1.
 // Blocked by panels of 16 columns: warp 0 factors a panel on its own (16 right-looking steps
-// with warp barriers, two rows per lane), then all threads apply the panel's rank-16 update to
-// the rows and columns after it; two CTA barriers per panel instead of two per column.
+// on the panel's columns held in registers, two rows per lane, each entry of the pivot column
+// passed to the other lanes by a shuffle), then all threads apply the panel's rank-16 update
+// to the rows and columns after it; two CTA barriers per panel instead of two per column.
 // =====================================================================================
 __global__ void __launch_bounds__(256) k_chol32(const float *__restrict__ G, float *__restrict__ Lout,
                                                 const int *skip) {
@@ -165,28 +166,44 @@ __global__ void __launch_bounds__(256) k_chol32(const float *__restrict__ G, flo
   for (int p = 0; p < kK / 16; ++p) {
     const int c0 = 16 * p, c1 = c0 + 16;
     if (tid < 32) {
-      for (int j = c0; j < c1; ++j) {
+      // the panel's 16 columns of rows lane and lane + 32 in registers; an entry of column j
+      // reaches the other lanes by a shuffle from the lane holding its row
+      const int ra = lane, rb = lane + 32;
+      float x0[16], x1[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        x0[k] = S[ra][c0 + k];
+        x1[k] = S[rb][c0 + k];
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int j = c0 + jj;
         // 1/sqrt(d) from the hardware estimate and one Newton step, sqrt(d) = d / sqrt(d)
-        const float d = S[j][j];
+        const float d = __shfl_sync(0xFFFFFFFFu, j < 32 ? x0[jj] : x1[jj], j & 31);
         float rp = 1.0f, piv = 1.0f;
         if (d > tiny) {
-          const float r0 = rsqrtf(d);
-          rp = r0 * fmaf(-0.5f * d * r0, r0, 1.5f);
+          const float q = rsqrtf(d);
+          rp = q * fmaf(-0.5f * d * q, q, 1.5f);
           piv = d * rp;
         }
-        __syncwarp();   // every lane has read the pivot
-        const int r0 = lane, r1 = lane + 32;
-        if (r0 > j) S[r0][j] *= rp;
-        if (r1 > j) S[r1][j] *= rp;
-        if (lane == 0) S[j][j] = piv;
-        __syncwarp();
-        // the panel's columns right of j
-        for (int c = j + 1; c < c1; ++c) {
-          const float lc = S[c][j];
-          if (r0 >= c) S[r0][c] = fmaf(-S[r0][j], lc, S[r0][c]);
-          if (r1 >= c) S[r1][c] = fmaf(-S[r1][j], lc, S[r1][c]);
+        if (ra > j) x0[jj] *= rp;
+        else if (ra == j) x0[jj] = piv;
+        if (rb > j) x1[jj] *= rp;
+        else if (rb == j) x1[jj] = piv;
+        // the panel's columns right of j: S[r][c] -= L[r][j] L[c][j] for r >= c
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          if (cc <= jj) continue;
+          const int c = c0 + cc;
+          const float lc = __shfl_sync(0xFFFFFFFFu, c < 32 ? x0[jj] : x1[jj], c & 31);
+          if (ra >= c) x0[cc] = fmaf(-x0[jj], lc, x0[cc]);
+          if (rb >= c) x1[cc] = fmaf(-x1[jj], lc, x1[cc]);
         }
-        __syncwarp();
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        S[ra][c0 + k] = x0[k];
+        S[rb][c0 + k] = x1[k];
       }
     }
     __syncthreads();
