@@ -224,6 +224,10 @@ gift_status gift_code_sizes(gift_format fmt, gift_scaling scaling, int d_out, in
  *  ws     : device workspace of gift_workspace_bytes(GIFT_OP_FACTOR_UPDATE, ..., T, ...)
  *           bytes (term planes of the activations and of Q, the partial sums, the FP64
  *           Cholesky scratch).
+ * LOWRANK with d_in > 64 allocates nothing, never waits on the host and enqueues the same
+ * launches on every call (once the Ritz residuals converge, the remaining launches return at
+ * once), so the call can be captured into a CUDA graph and replayed; a replay gives the eager
+ * call's factor bit for bit.
  * Returns INVALID_ARG on null pointers, T < 1, rank outside [1, min(32, d_in)]. */
 gift_status gift_factor_update(gift_ctx *ctx, gift_factor *f, const void *a, gift_dtype a_dt, int T,
                                const void *delta, gift_dtype d_dt, uint64_t seed, gift_precision prec,

@@ -265,3 +265,28 @@ def test_from_kfac_cholesky_bit_identical(kind):
     # and L L^T = A for the given A
     LA = f2.LA.cpu().double().numpy()
     assert rel_fro(LA @ LA.T, A.cpu().double().numpy()) <= 1e-5
+
+
+def test_refresh_replays_from_a_cuda_graph():
+    # the rank-r refresh is a fixed launch sequence that allocates nothing and never waits on
+    # the host (its convergence test only makes later launches return at once): captured
+    # once into a CUDA graph, a replay gives the eager call's factor bit for bit
+    spec = synth.LayerSpec("g", 128, 1024, T=4096, exponent=1.2, act_dtype=torch.bfloat16)
+    _, a = synth.layer_inputs(spec, 9, 3, 1, device="cuda")
+    n = G.gift_workspace_bytes(ctx(), "factor_update", "lowrank", "e4m3", "tensor", 128, 1024, a.shape[0], 32)
+    w = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    st = status()
+    eager = G.Factor.empty("lowrank", 128, 1024, 32)
+    G.gift_factor_update(ctx(), eager, a, seed=7, ws=w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    f = G.Factor.empty("lowrank", 128, 1024, 32)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        G.gift_factor_update(ctx(), f, a, seed=7, ws=w, status=st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for x, y in ((f.U, eager.U), (f.mu, eager.mu), (f.sigma, eager.sigma)):
+        assert torch.equal(x, y)
+    check_lowrank(f, a.double().cpu().numpy(), 32, 0)
